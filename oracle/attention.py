@@ -1,0 +1,317 @@
+"""fp64 reference definitions of the decode-attention hot path.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): imported by tests,
+``__graft_entry__.smoke()`` and the CPU-baseline legs of ``bench.py``; never by
+the library.
+
+Sources (the pages this library follows), cited by page title and section:
+
+* [KVC-LLM] "KV Cache 如何影响了 LLM Inference" (kakack.github.io),
+  §2.2 decode with a KV cache, §四 the unified MHA/GQA/MQA module
+  (difference 3: expand+reshape of K/V heads).
+* [ARG] "attention-variants-and-kv-cache" (arganzheng.life),
+  §二.1-2 decode attention, §三.2 GQA head grouping, §四.2-5 MLA structure,
+  decoupled RoPE and matrix absorption, §五.2 FlashAttention IO and the
+  flash-decoding split of the sequence with a merge of the normalisers,
+  §六.1 paging.
+* [MLA] "multi-head-latent-attention" (jianzhnie.github.io), §2 KV equations
+  (output with scale 1/sqrt(d_h + d_h^R)), §4 absorption.
+* [AIFAQ] aifaq.phimes.top, the decoupled-RoPE Q&A (cache = [c_kv ; k_rope],
+  score = content dot + rope dot).
+* [CH7] shippingwang.com ch.7 "KV Cache 优化", §7.3 (query head h reads KV
+  head h // g; never replicate, check the head axis).
+
+Readings where the pages are silent (listed again in the design doc):
+
+* RoPE: the pages state only that R_m depends on the position m and that
+  R_m^T R_n = R_{n-m} ([ARG] §四.4); the frequencies are deferred to another
+  article.  Reading: RoFormer-style rotation of interleaved coordinate pairs
+  (2i, 2i+1) by the angle pos * theta^(-2i/d_rot), theta = 10000, pos = the
+  token's 0-based slot.
+* The appended token's slot is the current length seqlens[b]; the caller
+  increments the length afterwards ([KVC-LLM] §2.2, [ARG] §二.2: the cache
+  only grows by one row per step).
+* Empty sequence: output 0, lse = -inf.  An empty split has weight 0.
+* Split partials are stored normalised (O_s = o_s / l_s) with
+  lse_s = m_s + ln l_s.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+PAGE = 64
+
+# ----------------------------------------------------------------------------
+# bf16 <-> fp64, from the bfloat16 format definition (1 sign bit, 8 exponent
+# bits, 7 stored mantissa bits: the top half of an IEEE binary32)
+# ----------------------------------------------------------------------------
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening: a bf16 bit pattern is the high 16 bits of a binary32."""
+    b = np.asarray(bits).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32).astype(np.float64)
+
+
+def bf16_to_f64(t) -> np.ndarray:
+    """torch bf16 tensor -> numpy float64 (exact)."""
+    import torch
+    return bf16_bits_to_f64(t.detach().to("cpu").contiguous()
+                            .view(torch.int16).numpy().view(np.uint16))
+
+
+def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float64 values to the nearest bf16 (ties to even) in one step,
+    returning uint16 bit patterns.  Finite normal inputs within bf16 range
+    (the only ones this library produces)."""
+    x = np.asarray(x, dtype=np.float64)
+    u = x.view(np.uint64)
+    # bf16 keeps 7 of binary64's 52 mantissa bits: drop 45 bits with RNE
+    drop = np.uint64(45)
+    lsb = (u >> drop) & np.uint64(1)
+    u = (u + (np.uint64(1) << (drop - np.uint64(1))) - np.uint64(1) + lsb)
+    u = u & ~((np.uint64(1) << drop) - np.uint64(1))
+    r = u.view(np.float64).astype(np.float32)   # exact: 8 significant bits
+    return (r.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+
+
+# ----------------------------------------------------------------------------
+# softmax attention of one query block over one key/value sequence
+# ----------------------------------------------------------------------------
+
+
+def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
+    """Single-step decode attention ([ARG] §二.1, [KVC-LLM] §2.2):
+    s_j = scale * q . K_j, p = softmax(s), out = sum_j p_j V_j,
+    lse = log sum_j exp(s_j).
+
+    q [H, dk], K [L, dk], V [L, dv] -> out [H, dv], lse [H].  L = 0 gives
+    out = 0 and lse = -inf."""
+    H = q.shape[0]
+    L = K.shape[0]
+    if L == 0:
+        return np.zeros((H, V.shape[1])), np.full(H, -np.inf)
+    s = scale * (q @ K.T)                       # [H, L]
+    m = s.max(axis=1, keepdims=True)
+    e = np.exp(s - m)
+    l = e.sum(axis=1, keepdims=True)
+    p = e / l
+    out = p @ V
+    lse = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+def gather_tokens(cache, b: int, L: int, block_table=None, head=None):
+    """Rows 0..L-1 of sequence b.  Contiguous caches are [B, heads, cap, d]
+    (head given) or [B, cap, d]; paged caches are [pages, heads, PAGE, d] or
+    [pages, PAGE, d] with token j at (block_table[b, j // PAGE], j % PAGE)
+    ([ARG] §六.1: the kernel looks up logical -> physical block)."""
+    j = np.arange(L)
+    if block_table is None:
+        return cache[b, head, :L] if head is not None else cache[b, :L]
+    pages = np.asarray(block_table)[b, j // PAGE]
+    if head is not None:
+        return cache[pages, head, j % PAGE]
+    return cache[pages, j % PAGE]
+
+
+def gqa_decode(q, k, v, seqlens, scale=None, block_table=None):
+    """MHA / GQA / MQA decode ([ARG] §三.2; [CH7] §7.3; [KVC-LLM] §四).
+
+    q [B, h, d]; k, v contiguous [B, n_kv, cap, d] or paged
+    [pages, n_kv, PAGE, d] with block_table [B, max_blocks].  Query head hh
+    reads KV head hh // g, g = h / n_kv.  Returns out [B, h, d], lse [B, h]
+    (natural log)."""
+    B, h, d = q.shape
+    n_kv = k.shape[1]
+    assert h % n_kv == 0
+    g = h // n_kv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out = np.zeros((B, h, d))
+    lse = np.zeros((B, h))
+    for b in range(B):
+        L = int(seqlens[b])
+        for hh in range(h):
+            kv = hh // g
+            K = gather_tokens(k, b, L, block_table, kv)
+            V = gather_tokens(v, b, L, block_table, kv)
+            o, l = attend(q[b, hh:hh + 1], K, V, scale)
+            out[b, hh] = o[0]
+            lse[b, hh] = l[0]
+    return out, lse
+
+
+def mla_decode_absorbed(q_abs, q_rope, cache, block_table, seqlens, scale=None):
+    """MLA decode with matrix absorption ([ARG] §四.5; [MLA] §4; [AIFAQ]).
+
+    Per head: score_j = scale * (q_abs . c_kv_j + q_rope . k_R_j) with the
+    cached row [c_kv (512) ; k_R (64)]; scale defaults to 1/sqrt(128 + 64)
+    (the pre-absorption head dim, not 1/sqrt(576)); the output stays in the
+    512-d latent space: out = sum_j p_j c_kv_j (V is the first 512 values of
+    the same cached row).  q_abs [B, n_h, 512], q_rope [B, n_h, 64],
+    cache [pages, PAGE, 576]."""
+    B, n_h, dc = q_abs.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(128 + 64)
+    out = np.zeros((B, n_h, dc))
+    lse = np.zeros((B, n_h))
+    for b in range(B):
+        L = int(seqlens[b])
+        rows = gather_tokens(cache, b, L, block_table)       # [L, 576]
+        c_kv, k_r = rows[:, :dc], rows[:, dc:]
+        if L == 0:
+            lse[b] = -np.inf
+            continue
+        s = scale * (q_abs[b] @ c_kv.T + q_rope[b] @ k_r.T)   # content + rope
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        l = e.sum(axis=1, keepdims=True)
+        out[b] = (e / l) @ c_kv
+        lse[b] = (m + np.log(l))[:, 0]
+    return out, lse
+
+
+def mla_decode_nonabsorbed(q_nope, q_rope, cache, block_table, seqlens,
+                           W_UK, W_UV, scale=None):
+    """The literal (prefill-style) MLA path ([ARG] §四.2 and the §四.5
+    figure; [MLA] §2): up-project every cached latent to per-head keys and
+    values, k^C_{j,h} = W_UK,h c_kv_j and v^C_{j,h} = W_UV,h c_kv_j with
+    W_UK [n_h, d_h, 512] and W_UV [n_h, d_v, 512] (column-vector form, W_UK,h
+    being head h's 128x512 block), then standard attention of
+    q = [q^C ; q^R] against k = [k^C ; k^R] with values v^C.
+    Returns the per-head output in value space [B, n_h, d_v]."""
+    B, n_h, dh = q_nope.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(dh + q_rope.shape[2])
+    dv = W_UV.shape[1]
+    out = np.zeros((B, n_h, dv))
+    lse = np.zeros((B, n_h))
+    for b in range(B):
+        L = int(seqlens[b])
+        rows = gather_tokens(cache, b, L, block_table)
+        c_kv, k_r = rows[:, :512], rows[:, 512:]
+        for hh in range(n_h):
+            kC = c_kv @ W_UK[hh].T                    # [L, d_h]
+            vC = c_kv @ W_UV[hh].T                    # [L, d_v]
+            K = np.concatenate([kC, k_r], axis=1)
+            qf = np.concatenate([q_nope[b, hh], q_rope[b, hh]])[None]
+            o, l = attend(qf, K, vC, scale)
+            out[b, hh] = o[0]
+            lse[b, hh] = l[0]
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# flash-decoding split and merge ([ARG] §五.2, last paragraph: split the KV
+# along the sequence, softmax each piece locally, then merge the normalisers)
+# ----------------------------------------------------------------------------
+
+
+def split_partials(q, K, V, scale, bounds):
+    """Local softmax over each token range [bounds[s], bounds[s+1]):
+    normalised partial outputs O_s [S, H, dv] and lse_s [S, H]."""
+    S = len(bounds) - 1
+    H = q.shape[0]
+    O = np.zeros((S, H, V.shape[1]))
+    lse = np.zeros((S, H))
+    for s in range(S):
+        a, e = bounds[s], bounds[s + 1]
+        O[s], lse[s] = attend(q, K[a:e], V[a:e], scale)
+    return O, lse
+
+
+def combine_splits(partial_o, partial_lse, counts=None):
+    """Merge S normalised partials per row: M = max_s lse_s,
+    w_s = exp(lse_s - M), out = sum_s w_s O_s / sum_s w_s,
+    lse = M + ln sum_s w_s.  partial_o [S, R, D], partial_lse [S, R];
+    counts [R] limits row r to its first counts[r] partials (None: all S).
+    Rows whose partials are all empty get out = 0, lse = -inf."""
+    S, R, D = partial_o.shape
+    out = np.zeros((R, D))
+    lse = np.full(R, -np.inf)
+    for r in range(R):
+        n = S if counts is None else int(counts[r])
+        ls = partial_lse[:n, r]
+        if n == 0 or not np.isfinite(ls).any():
+            continue
+        M = ls.max()
+        w = np.exp(ls - M)
+        out[r] = (w[:, None] * partial_o[:n, r]).sum(axis=0) / w.sum()
+        lse[r] = M + math.log(w.sum())
+    return out, lse
+
+
+# ----------------------------------------------------------------------------
+# rotary position embedding and the cache append
+# ----------------------------------------------------------------------------
+
+
+def rope_matrix(pos: float, dim: int, theta: float = 10000.0) -> np.ndarray:
+    """The block-diagonal rotation R_pos (reading: interleaved pairs,
+    angle_i = pos * theta^(-2i/dim)).  Used by the tests to check
+    R_m^T R_n = R_{n-m} ([ARG] §四.4)."""
+    R = np.zeros((dim, dim))
+    for i in range(dim // 2):
+        a = pos * theta ** (-2.0 * i / dim)
+        c, s = math.cos(a), math.sin(a)
+        R[2 * i, 2 * i], R[2 * i, 2 * i + 1] = c, -s
+        R[2 * i + 1, 2 * i], R[2 * i + 1, 2 * i + 1] = s, c
+    return R
+
+
+def rope_rotate(x: np.ndarray, pos, theta: float = 10000.0) -> np.ndarray:
+    """Rotate the last axis of x (interleaved pairs) to position(s) ``pos``
+    (broadcast over the leading axes)."""
+    x = np.asarray(x, dtype=np.float64)
+    dim = x.shape[-1]
+    i = np.arange(dim // 2)
+    inv = theta ** (-2.0 * i / dim)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * inv
+    c, s = np.cos(ang), np.sin(ang)
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    y = np.empty_like(x)
+    y[..., 0::2] = x0 * c - x1 * s
+    y[..., 1::2] = x0 * s + x1 * c
+    return y
+
+
+def append_rope_mla(cache_bits, block_table, seqlens, c_kv_bits, kr_bits,
+                    theta=10000.0):
+    """Write one new token per sequence into the paged latent cache
+    ([ARG] §四.2: c_kv is cached as is, k_R is cached already rotated;
+    [KVC-LLM] §2.2: the cache grows by one row).  All arrays are bf16 bit
+    patterns (uint16).  Slot: pos = seqlens[b], page block_table[b, pos//64],
+    row pos % 64.  Returns a new cache array."""
+    out = np.array(cache_bits, copy=True)
+    for b in range(len(seqlens)):
+        pos = int(seqlens[b])
+        page = int(block_table[b, pos // PAGE])
+        row = pos % PAGE
+        out[page, row, :512] = c_kv_bits[b]
+        rot = rope_rotate(bf16_bits_to_f64(kr_bits[b]), pos, theta)
+        out[page, row, 512:] = f64_to_bf16_bits(rot)
+    return out
+
+
+def append_rope_gqa(k_bits, v_bits, seqlens, k_new_bits, v_new_bits,
+                    block_table=None, theta=10000.0):
+    """GQA cache append: K[.., pos, :] = RoPE_pos(k_new) over the whole head
+    dim, V[.., pos, :] = v_new.  Contiguous [B, n_kv, cap, d] or paged
+    [pages, n_kv, PAGE, d] layouts; bf16 bit patterns in and out."""
+    K = np.array(k_bits, copy=True)
+    V = np.array(v_bits, copy=True)
+    B, n_kv, d = k_new_bits.shape
+    for b in range(B):
+        pos = int(seqlens[b])
+        rot = f64_to_bf16_bits(rope_rotate(bf16_bits_to_f64(k_new_bits[b]), pos, theta))
+        if block_table is None:
+            K[b, :, pos] = rot
+            V[b, :, pos] = v_new_bits[b]
+        else:
+            page = int(block_table[b, pos // PAGE])
+            K[page, :, pos % PAGE] = rot
+            V[page, :, pos % PAGE] = v_new_bits[b]
+    return K, V

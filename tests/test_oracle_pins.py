@@ -1,0 +1,395 @@
+"""Pins for the fp64 oracle: each test ties an oracle function to something
+other than itself -- values the pages print, hand-worked examples, closed
+forms, special cases with a known answer, and invariants the pages state.
+CPU only."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+import oracle
+from oracle import closed_forms as cf
+from conftest import read_golden
+
+RNG = np.random.default_rng(20261202)
+
+
+# ---------------------------------------------------------------- worked examples
+
+def test_two_token_hand_example():
+    g = read_golden("two_token_hand.txt")
+    q = np.array([g["q"]])
+    K = np.array([g["k0"], g["k1"]])
+    V = np.array([g["v0"], g["v1"]])
+    out, lse = oracle.attend(q, K, V, 1.0)
+    np.testing.assert_allclose(out[0], g["out"], rtol=0, atol=1e-14)
+    assert abs(lse[0] - g["lse"][0]) < 1e-14
+
+
+def test_gqa_hand_example_head_mapping():
+    g = read_golden("gqa_hand.txt")
+    q = np.ones((1, 4, 1))
+    k = np.zeros((1, 2, 2, 1))
+    v = np.zeros((1, 2, 2, 1))
+    v[0, 0, :, 0] = g["v_head0"]
+    v[0, 1, :, 0] = g["v_head1"]
+    out, lse = oracle.gqa_decode(q, k, v, [2], scale=1.0)
+    np.testing.assert_allclose(out[0, :, 0], g["out"], atol=1e-14)
+    np.testing.assert_allclose(lse[0], g["lse"][0] * np.ones(4), atol=1e-14)
+    # the wrong (tiled) head mapping is distinguishable on this example
+    assert not np.allclose(out[0, :, 0], [3, 20, 3, 20])
+
+
+# ---------------------------------------------------------------- special cases
+
+def test_single_token_returns_its_value_row():
+    q = RNG.normal(size=(3, 16))
+    K = RNG.normal(size=(1, 16))
+    V = RNG.normal(size=(1, 8))
+    out, lse = oracle.attend(q, K, V, 0.25)
+    np.testing.assert_allclose(out, np.repeat(V, 3, 0), atol=1e-15)
+    np.testing.assert_allclose(lse, 0.25 * q @ K[0], atol=1e-14)
+
+
+def test_equal_keys_average_values():
+    L = 37
+    q = RNG.normal(size=(2, 8))
+    K = np.repeat(RNG.normal(size=(1, 8)), L, 0)
+    V = RNG.normal(size=(L, 5))
+    out, lse = oracle.attend(q, K, V, 0.5)
+    np.testing.assert_allclose(out, np.repeat(V.mean(0, keepdims=True), 2, 0), atol=1e-13)
+    np.testing.assert_allclose(lse, 0.5 * q @ K[0] + math.log(L), atol=1e-12)
+
+
+def test_dominant_key_selects_its_value():
+    L, d = 20, 8
+    q = RNG.normal(size=(1, d))
+    K = RNG.normal(size=(L, d)) * 0.01
+    K[13] = 60.0 * q[0] / np.linalg.norm(q[0]) ** 2   # score 60 vs ~0
+    V = RNG.normal(size=(L, 4))
+    out, _ = oracle.attend(q, K, V, 1.0)
+    np.testing.assert_allclose(out[0], V[13], atol=1e-12)
+
+
+def test_probabilities_sum_to_one():
+    q = RNG.normal(size=(4, 32))
+    K = RNG.normal(size=(300, 32))
+    out, _ = oracle.attend(q, K, np.ones((300, 3)), 1 / math.sqrt(32))
+    np.testing.assert_allclose(out, 1.0, atol=1e-12)
+
+
+def test_empty_sequence():
+    out, lse = oracle.attend(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 3)), 1.0)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_brute_force_tiny_gqa():
+    """Scalar loops (math.exp) on a tiny GQA problem with ragged lengths."""
+    B, h, n_kv, d = 2, 4, 2, 3
+    q = RNG.normal(size=(B, h, d))
+    k = RNG.normal(size=(B, n_kv, 5, d))
+    v = RNG.normal(size=(B, n_kv, 5, d))
+    sl = [5, 2]
+    out, lse = oracle.gqa_decode(q, k, v, sl, scale=0.7)
+    for b in range(B):
+        for hh in range(h):
+            kv = hh // 2
+            s = [0.7 * sum(q[b, hh, i] * k[b, kv, j, i] for i in range(d)) for j in range(sl[b])]
+            z = sum(math.exp(x) for x in s)
+            for i in range(d):
+                ref = sum(math.exp(s[j]) / z * v[b, kv, j, i] for j in range(sl[b]))
+                assert abs(out[b, hh, i] - ref) < 1e-13
+            assert abs(lse[b, hh] - math.log(z)) < 1e-13
+
+
+# ---------------------------------------------------------------- GQA invariants
+
+def test_repeat_kv_equals_mha():
+    """[KVC-LLM] §四 (difference 3) and [CH7] §7.3: expanding each KV head g
+    times along the head axis turns GQA into MHA with the same result."""
+    B, h, n_kv, d, L = 2, 8, 2, 16, 40
+    q = RNG.normal(size=(B, h, d))
+    k = RNG.normal(size=(B, n_kv, L, d))
+    v = RNG.normal(size=(B, n_kv, L, d))
+    sl = [40, 23]
+    o1, l1 = oracle.gqa_decode(q, k, v, sl)
+    kr = np.repeat(k, h // n_kv, axis=1)
+    vr = np.repeat(v, h // n_kv, axis=1)
+    o2, l2 = oracle.gqa_decode(q, kr, vr, sl)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    # MQA is the g = h end of the same family
+    o3, _ = oracle.gqa_decode(q, k[:, :1], v[:, :1], sl)
+    o4, _ = oracle.gqa_decode(q, np.repeat(k[:, :1], h, 1), np.repeat(v[:, :1], h, 1), sl)
+    np.testing.assert_array_equal(o3, o4)
+
+
+def test_head_axis_detector():
+    """[CH7] §7.3: a broadcast on the wrong axis keeps shapes but breaks the
+    logits.  Give each KV head a distinct constant value; head hh must read
+    KV head hh // g."""
+    B, h, n_kv, d, L = 1, 12, 3, 4, 9
+    q = RNG.normal(size=(B, h, d))
+    k = RNG.normal(size=(B, n_kv, L, d))
+    v = np.zeros((B, n_kv, L, d))
+    for kv in range(n_kv):
+        v[:, kv] = kv + 1
+    out, _ = oracle.gqa_decode(q, k, v, [L])
+    np.testing.assert_allclose(out[0, :, 0], [hh // 4 + 1 for hh in range(h)], atol=1e-13)
+
+
+def test_paged_equals_contiguous():
+    """[ARG] §六.1: paging only changes where a token lives."""
+    case = kvgen.gqa_case(3, 4, 2, 16, seqlens=[130, 64, 1], paged=True, seed=7)
+    k = oracle.bf16_to_f64(case.k)
+    v = oracle.bf16_to_f64(case.v)
+    q = oracle.bf16_to_f64(case.q)
+    bt = case.block_table.numpy()
+    sl = case.seqlens.numpy()
+    cap = bt.shape[1] * 64
+    kc = np.zeros((3, 2, cap, 16))
+    vc = np.zeros((3, 2, cap, 16))
+    for b in range(3):
+        for j in range(sl[b]):
+            kc[b, :, j] = k[bt[b, j // 64], :, j % 64]
+            vc[b, :, j] = v[bt[b, j // 64], :, j % 64]
+    o1, l1 = oracle.gqa_decode(q, k, v, sl, block_table=bt)
+    o2, l2 = oracle.gqa_decode(q, kc, vc, sl)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+# ---------------------------------------------------------------- split / combine
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7, 61])
+def test_split_invariance(S):
+    """[ARG] §五.2: softmax pieces merge exactly by their normalisers."""
+    L = 61
+    q = RNG.normal(size=(5, 24))
+    K = RNG.normal(size=(L, 24))
+    V = RNG.normal(size=(L, 10))
+    ref, lref = oracle.attend(q, K, V, 0.3)
+    bounds = [round(i * L / S) for i in range(S + 1)]
+    O, ls = oracle.split_partials(q, K, V, 0.3, bounds)
+    out, lse = oracle.combine_splits(O, ls)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, atol=1e-12)
+
+
+def test_combine_with_empty_split_and_counts():
+    q = RNG.normal(size=(2, 8))
+    K = RNG.normal(size=(10, 8))
+    V = RNG.normal(size=(10, 3))
+    ref, lref = oracle.attend(q, K, V, 1.0)
+    # three splits, the middle one empty, plus one trailing unused slot
+    O, ls = oracle.split_partials(q, K, V, 1.0, [0, 4, 4, 10])
+    assert np.all(np.isneginf(ls[1]))
+    O = np.concatenate([O, np.full((1, 2, 3), 1e30)])
+    ls = np.concatenate([ls, np.full((1, 2), 50.0)])
+    out, lse = oracle.combine_splits(O, ls, counts=[3, 3])
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, atol=1e-12)
+    out0, lse0 = oracle.combine_splits(O, ls, counts=[0, 3])
+    assert np.all(out0[0] == 0) and np.isneginf(lse0[0])
+
+
+# ---------------------------------------------------------------- MLA
+
+def _mla_small(B=2, n_h=4, sl=(70, 9)):
+    case = kvgen.mla_case(B, n_h, seqlens=list(sl), seed=11)
+    return (oracle.bf16_to_f64(case.q_abs), oracle.bf16_to_f64(case.q_rope),
+            oracle.bf16_to_f64(case.cache), case.block_table.numpy(),
+            case.seqlens.numpy())
+
+
+def test_mla_absorbed_equals_nonabsorbed():
+    """[ARG] §四.5 and [MLA] §4: q~_h = W_UK,h^T q^C_h against the latent
+    gives the same scores as up-projecting every cached latent; applying
+    W_UV,h to the latent output gives the standard per-head output; the
+    scale stays 1/sqrt(128 + 64)."""
+    _, q_rope, cache, bt, sl = _mla_small()
+    B, n_h = q_rope.shape[:2]
+    W_UK = RNG.normal(size=(n_h, 128, 512)) / math.sqrt(512)
+    W_UV = RNG.normal(size=(n_h, 128, 512)) / math.sqrt(512)
+    q_nope = RNG.normal(size=(B, n_h, 128))
+    q_abs = np.einsum("bhd,hdc->bhc", q_nope, W_UK)
+    lat, lse_a = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl)
+    o_abs = np.einsum("hvc,bhc->bhv", W_UV, lat)
+    o_ref, lse_n = oracle.mla_decode_nonabsorbed(q_nope, q_rope, cache, bt, sl, W_UK, W_UV)
+    np.testing.assert_allclose(o_abs, o_ref, atol=1e-11)
+    np.testing.assert_allclose(lse_a, lse_n, atol=1e-11)
+    # 1/sqrt(576) is a different (wrong) reading and shows up
+    lat2, _ = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl, scale=1 / 24.0)
+    assert not np.allclose(lat2, lat, atol=1e-6)
+
+
+def test_mla_score_is_concatenated_dot():
+    """[AIFAQ]: [q_c ; q_r] . [k_c ; k_r] = q_c.k_c + q_r.k_r, and V is the
+    first 512 values of the same cached row ([ARG] §四.5): MLA equals one
+    MQA head of key dim 576 and value dim 512."""
+    q_abs, q_rope, cache, bt, sl = _mla_small()
+    lat, lse = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl)
+    for b in range(len(sl)):
+        rows = oracle.gather_tokens(cache, b, int(sl[b]), bt)
+        qf = np.concatenate([q_abs[b], q_rope[b]], axis=1)
+        o, l = oracle.attend(qf, rows, rows[:, :512], 1 / math.sqrt(192))
+        np.testing.assert_allclose(lat[b], o, atol=1e-12)
+        np.testing.assert_allclose(lse[b], l, atol=1e-12)
+
+
+def test_mla_rope_term_matters():
+    q_abs, q_rope, cache, bt, sl = _mla_small()
+    a, _ = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl)
+    b, _ = oracle.mla_decode_absorbed(q_abs, 0 * q_rope, cache, bt, sl)
+    assert not np.allclose(a, b, atol=1e-6)
+
+
+def test_mla_single_token():
+    q_abs, q_rope, cache, bt, _ = _mla_small()
+    lat, _ = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, np.array([1, 1]))
+    for b in range(2):
+        np.testing.assert_allclose(lat[b], np.repeat(cache[bt[b, 0], 0:1, :512], 4, 0), atol=0)
+
+
+# ---------------------------------------------------------------- RoPE
+
+def test_rope_identity_at_zero_and_norm():
+    x = RNG.normal(size=(5, 64))
+    np.testing.assert_array_equal(oracle.rope_rotate(x, np.zeros(5)), x)
+    y = oracle.rope_rotate(x, np.arange(5) * 1000.0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-13)
+
+
+def test_rope_relative_position():
+    """[ARG] §四.4: R_m^T R_n = R_{n-m}, so <R_m q, R_n k> depends on n - m."""
+    for m, n in [(3, 10), (100, 4), (131000, 131072)]:
+        Rm, Rn, Rd = (oracle.rope_matrix(p, 8) for p in (m, n, n - m))
+        np.testing.assert_allclose(Rm.T @ Rn, Rd, atol=1e-9)
+    q, k = RNG.normal(size=64), RNG.normal(size=64)
+    a = oracle.rope_rotate(q, 17.0) @ oracle.rope_rotate(k, 29.0)
+    b = oracle.rope_rotate(q, 1017.0) @ oracle.rope_rotate(k, 1029.0)
+    assert abs(a - b) < 1e-10
+
+
+def test_rope_known_angles():
+    """Reading: interleaved pairs, angle_i = pos * theta^(-2i/dim)."""
+    y = oracle.rope_rotate(np.array([1.0, 0.0]), 1.0)
+    np.testing.assert_allclose(y, [math.cos(1), math.sin(1)], atol=1e-16)
+    y = oracle.rope_rotate(np.array([0.0, 0.0, 1.0, 0.0]), 100.0)   # 10000^(-2/4) = 1/100
+    np.testing.assert_allclose(y, [0, 0, math.cos(1), math.sin(1)], atol=1e-15)
+    y = oracle.rope_rotate(np.array([0.0, 1.0]), math.pi / 2)
+    np.testing.assert_allclose(y, [-1, 0], atol=1e-15)
+
+
+# ---------------------------------------------------------------- bf16 rounding
+
+def test_bf16_rounding_known_values():
+    f = oracle.f64_to_bf16_bits
+    assert f(np.array([1.0]))[0] == 0x3F80
+    assert f(np.array([1.0 + 2 ** -8]))[0] == 0x3F80          # tie -> even
+    assert f(np.array([1.0 + 3 * 2 ** -8]))[0] == 0x3F82      # tie -> even (up)
+    assert f(np.array([1.0 + 2 ** -8 + 2 ** -30]))[0] == 0x3F81
+    assert f(np.array([-2.0]))[0] == 0xC000
+
+
+def test_bf16_rounding_matches_fp32_cast():
+    """One RNE step from binary32 (a library routine) is the special case of
+    the fp64 rounding for inputs that are exact binary32 values."""
+    x = torch.randn(100000, dtype=torch.float32) * 3
+    ref = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.f64_to_bf16_bits(x.numpy().astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+    back = oracle.bf16_bits_to_f64(ref)
+    np.testing.assert_array_equal(back, x.to(torch.bfloat16).to(torch.float64).numpy())
+
+
+# ---------------------------------------------------------------- cache append
+
+def test_append_mla_slot_and_rotation():
+    sl = np.array([0, 63, 64, 200])
+    case = kvgen.mla_case(4, 2, seqlens=[1, 64, 65, 201], seed=3, spare_pages=2)
+    bits = case.cache.view(torch.int16).numpy().view(np.uint16)
+    bt = case.block_table.numpy()
+    ckv, kr = kvgen.append_inputs_mla(4, seed=5)
+    cb = ckv.view(torch.int16).numpy().view(np.uint16)
+    kb = kr.view(torch.int16).numpy().view(np.uint16)
+    new = oracle.append_rope_mla(bits, bt, sl, cb, kb)
+    changed = np.argwhere(np.any(new != bits, axis=2))
+    expect = {(int(bt[b, sl[b] // 64]), int(sl[b] % 64)) for b in range(4)}
+    assert {tuple(x) for x in changed} <= expect
+    for b in range(4):
+        page, row = bt[b, sl[b] // 64], sl[b] % 64
+        np.testing.assert_array_equal(new[page, row, :512], cb[b])
+        back = oracle.rope_rotate(oracle.bf16_bits_to_f64(new[page, row, 512:]), -float(sl[b]))
+        np.testing.assert_allclose(back, oracle.bf16_bits_to_f64(kb[b]), atol=0.02)
+    # position 0 is the identity rotation
+    np.testing.assert_array_equal(new[bt[0, 0], 0, 512:], kb[0])
+
+
+def test_append_gqa_contiguous_and_paged():
+    sl = np.array([5, 0])
+    k_new, v_new = kvgen.append_inputs_gqa(2, 2, 8, seed=9)
+    kn = k_new.view(torch.int16).numpy().view(np.uint16)
+    vn = v_new.view(torch.int16).numpy().view(np.uint16)
+    K = np.zeros((2, 2, 16, 8), np.uint16)
+    V = np.zeros((2, 2, 16, 8), np.uint16)
+    K2, V2 = oracle.append_rope_gqa(K, V, sl, kn, vn)
+    np.testing.assert_array_equal(V2[0, :, 5], vn[0])
+    np.testing.assert_array_equal(K2[1, :, 0], kn[1])       # pos 0: no rotation
+    rot = oracle.rope_rotate(oracle.bf16_bits_to_f64(kn[0]), 5.0)
+    np.testing.assert_array_equal(K2[0, :, 5], oracle.f64_to_bf16_bits(rot))
+    mask = np.ones(K.shape, bool)
+    mask[0, :, 5] = False
+    mask[1, :, 0] = False
+    assert np.all(K2[mask] == 0) and np.all(V2[mask] == 0)
+    bt = np.array([[1, 0], [2, 3]])
+    Kp = np.zeros((4, 2, 64, 8), np.uint16)
+    Vp = np.zeros((4, 2, 64, 8), np.uint16)
+    Kp2, Vp2 = oracle.append_rope_gqa(Kp, Vp, np.array([70, 3]), kn, vn, block_table=bt)
+    np.testing.assert_array_equal(Vp2[0, :, 6], vn[0])
+    np.testing.assert_array_equal(Vp2[2, :, 3], vn[1])
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_closed_forms_match_printed_values():
+    g = {k: v[0] for k, v in read_golden("cache_sizes.txt").items()}
+    mla = cf.kv_elems_per_token_per_layer("mla", d_c=512, d_rope=64)
+    assert mla == g["mla_elems_per_token_per_layer"]
+    assert 64 / 512 == g["mla_rope_overhead"]
+    mha5120 = cf.kv_elems_per_token_per_layer("mha", n_heads=40, head_dim=128)
+    assert round(mha5120 / mla, 1) == g["mha_vs_mla_ratio_dmodel5120"]
+    assert mha5120 / 512 == g["mha_vs_pure_mla_ratio_dmodel5120"]
+    assert cf.kv_bytes_per_token(60, mla) == g["mla_60_layer_bytes_per_token"]
+    assert cf.kv_bytes_per_token(60, mla) / 1024 == 67.5
+    assert cf.kv_elems_per_token_per_layer("mha", n_heads=32, head_dim=128) == g["llama2_mha_elems"]
+    assert cf.kv_elems_per_token_per_layer("gqa", n_kv_heads=8, head_dim=128) == g["llama2_gqa8_elems"]
+    assert cf.kv_elems_per_token_per_layer("mqa", head_dim=128) == g["llama2_mqa_elems"]
+    assert cf.kv_elems_per_token_per_layer("mla", d_c=512) == g["llama2_mla_elems"]
+    l8 = cf.kv_elems_per_token_per_layer("gqa", n_kv_heads=8, head_dim=128)
+    assert cf.kv_bytes_per_token(32, l8) == g["llama3_8b_gqa_bytes_per_token"]
+    l8m = cf.kv_elems_per_token_per_layer("mha", n_heads=32, head_dim=128)
+    assert cf.kv_bytes_per_token(32, l8m) == g["llama3_8b_mha_bytes_per_token"]
+    assert cf.kv_bytes_per_token(80, l8) == g["llama3_70b_gqa_bytes_per_token"]
+    v3 = cf.kv_bytes_per_token(61, mla)
+    assert v3 == g["deepseek_v3_mla_bytes_per_token"]
+    v3m = cf.kv_bytes_per_token(61, cf.kv_elems_per_token_per_layer("mha", n_heads=128, head_dim=128))
+    assert v3m == g["deepseek_v3_as_mha_bytes_per_token"]
+    assert round(v3m / v3, 1) == g["deepseek_v3_mha_over_mla"]
+    gib = 1024 ** 3
+    assert round(131072 * 131072 / gib, 1) == g["llama3_8b_128k_gib"]
+    assert round(327680 * 131072 / gib, 1) == g["llama3_70b_128k_gib"]
+    assert round(v3 * 131072 / gib, 1) == g["deepseek_v3_128k_gib"]
+    assert cf.decode_intensity("mha", 32, l8m, head_dim=128) == g["intensity_mha"]
+    assert cf.decode_intensity("gqa", 32, l8, head_dim=128) == g["intensity_llama3_8b"]
+    assert cf.decode_intensity("gqa", 64, l8, head_dim=128) == g["intensity_llama3_70b"]
+    assert round(cf.decode_intensity("mla", 128, mla, d_c=512, d_rope=64)) == g["intensity_deepseek_v3"]
+    assert cf.mla_flops_per_token(128) == g["mla_flops_per_token_per_layer"]
+    assert mla * 2 == g["mla_bytes_per_token_per_layer"]
+    assert l8 * 2 == g["llama3_8b_gqa_bytes_per_token_per_layer"]
+    assert 32 * 2 * 256 == g["llama3_8b_gqa_flops_per_token_per_layer"]
+    assert 192 + 128 == g["dot_len_unabsorbed"] and 576 + 512 == g["dot_len_absorbed"]
+    assert round(cf.mla_vs_mha_read_ratio(20), 2) == g["mla_mha_read_ratio_s20"]
+    assert abs(cf.mla_vs_mha_read_ratio(1e12) - g["mla_mha_read_ratio_limit"]) < 1e-9

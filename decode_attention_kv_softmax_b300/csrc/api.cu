@@ -1,0 +1,353 @@
+// Host side of the C ABI declared in include/kvdec.h: argument checks,
+// workspace layout, TMA tensor-map encoding and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "common.cuh"
+
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+kvdec_status fail(kvdec_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvdec_status fail(kvdec_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return s;
+}
+
+kvdec_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(KVDEC_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- devices
+
+struct DeviceInfo {
+    int sm_count = 0;
+};
+
+std::mutex g_mu;
+std::map<int, DeviceInfo> g_devices;
+std::map<std::tuple<int, int, int, int, int>, int> g_occupancy;  // (dev, kind, D, MT, B)
+
+bool device_info(DeviceInfo& out, int& dev) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_devices.find(dev);
+    if (it != g_devices.end()) {
+        out = it->second;
+        return true;
+    }
+    DeviceInfo d;
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return false;
+    g_devices[dev] = d;
+    out = d;
+    return true;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, box of
+// box_cols x box_rows elements, given swizzle.
+kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                       uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
+                       CUtensorMapSwizzle swz) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {row_stride_bytes};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return KVDEC_OK;
+}
+
+// ---------------------------------------------------------------- GQA layout
+
+struct GqaPlan {
+    int D, MT, g, n_hc, hc_rows, units;
+    int grid;
+    size_t off_lse, off_o, bytes;
+};
+
+constexpr int kMaxBatch = 8192;
+
+// Call epoch for the split-piece counters (see arrive_piece): kept in
+// [1, 2^23) so that a counter word never looks like a normal float pair.
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> e{0};
+    return (e.fetch_add(1, std::memory_order_relaxed) % ((1u << 23) - 1u)) + 1u;
+}
+
+kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1 || p->batch > kMaxBatch)
+        return fail(KVDEC_ERR_INVALID_ARG, "batch %d outside [1, %d]", p->batch, kMaxBatch);
+    if (p->num_heads < 1 || p->num_kv_heads < 1 || p->num_heads % p->num_kv_heads)
+        return fail(KVDEC_ERR_INVALID_ARG, "num_heads %d must be a positive multiple of num_kv_heads %d",
+                    p->num_heads, p->num_kv_heads);
+    if (p->head_dim != 64 && p->head_dim != 128)
+        return fail(KVDEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", p->head_dim);
+    pl.D = p->head_dim;
+    pl.g = p->num_heads / p->num_kv_heads;
+    pl.hc_rows = pl.g <= 32 ? pl.g : 32;
+    pl.n_hc = (pl.g + pl.hc_rows - 1) / pl.hc_rows;
+    pl.MT = pl.hc_rows > 16 ? 2 : 1;
+    pl.units = p->batch * p->num_kv_heads * pl.n_hc;
+    DeviceInfo di;
+    int dev;
+    if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
+    int occ;
+    {
+        auto key = std::make_tuple(dev, 0, pl.D, pl.MT, p->batch);
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it == g_occupancy.end()) {
+            occ = kvdec::occupancy_gqa(pl.D, pl.MT, p->batch);
+            g_occupancy[key] = occ;
+        } else {
+            occ = it->second;
+        }
+    }
+    if (occ < 1) return fail(KVDEC_ERR_CUDA, "GQA kernel does not fit on this device");
+    pl.grid = di.sm_count * occ;
+    if (p->max_ctas > 0 && p->max_ctas < pl.grid) pl.grid = p->max_ctas;
+    const size_t slots = 2 * (size_t)pl.grid;
+    pl.off_lse = round_up((size_t)pl.units * 8, 256);
+    pl.off_o = pl.off_lse + round_up(slots * pl.hc_rows * 4, 256);
+    pl.bytes = pl.off_o + slots * pl.hc_rows * pl.D * 4;
+    return KVDEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvdec_abi_version(void) { return KVDEC_ABI_VERSION; }
+
+int64_t kvdec_params_size(int kind) {
+    switch (kind) {
+        case 0: return (int64_t)sizeof(kvdec_gqa_params);
+        case 1: return (int64_t)sizeof(kvdec_mla_params);
+        case 2: return (int64_t)sizeof(kvdec_append_params);
+        case 3: return (int64_t)sizeof(kvdec_combine_params);
+        default: return -1;
+    }
+}
+
+const char* kvdec_status_string(kvdec_status s) {
+    switch (s) {
+        case KVDEC_OK: return "ok";
+        case KVDEC_ERR_INVALID_ARG: return "invalid argument";
+        case KVDEC_ERR_UNSUPPORTED: return "unsupported";
+        case KVDEC_ERR_CUDA: return "CUDA error";
+        case KVDEC_ERR_WORKSPACE: return "workspace too small";
+        default: return "unknown status";
+    }
+}
+
+const char* kvdec_last_error(void) { return g_last_error.c_str(); }
+
+size_t kvdec_gqa_workspace_bytes(const kvdec_gqa_params* p) {
+    GqaPlan pl;
+    if (plan_gqa(p, pl) != KVDEC_OK) return 0;
+    return pl.bytes;
+}
+
+kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
+    GqaPlan pl;
+    kvdec_status st = plan_gqa(p, pl);
+    if (st != KVDEC_OK) return st;
+    if (!p->q || !p->k || !p->v || !p->seqlens || !p->out)
+        return fail(KVDEC_ERR_INVALID_ARG, "q, k, v, seqlens and out must be non-NULL");
+    if (!aligned(p->q, 16) || !aligned(p->k, 16) || !aligned(p->v, 16) || !aligned(p->out, 16))
+        return fail(KVDEC_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (!aligned(p->seqlens, 4) || (p->lse && !aligned(p->lse, 4)))
+        return fail(KVDEC_ERR_INVALID_ARG, "seqlens and lse must be 4-byte aligned");
+    if (p->out_dtype != KVDEC_F32 && p->out_dtype != KVDEC_BF16)
+        return fail(KVDEC_ERR_INVALID_ARG, "out_dtype %d", p->out_dtype);
+    if (!p->workspace || !aligned(p->workspace, 256))
+        return fail(KVDEC_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+    if (p->workspace_bytes < pl.bytes)
+        return fail(KVDEC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", p->workspace_bytes,
+                    pl.bytes);
+    const bool paged = p->block_table != nullptr;
+    uint64_t rows;
+    int cap;
+    if (paged) {
+        if (p->num_pages < 1 || p->max_blocks < 1)
+            return fail(KVDEC_ERR_INVALID_ARG, "paged cache needs num_pages >= 1 and max_blocks >= 1");
+        if (!aligned(p->block_table, 4)) return fail(KVDEC_ERR_INVALID_ARG, "block_table alignment");
+        rows = (uint64_t)p->num_pages * p->num_kv_heads * KVDEC_PAGE_SIZE;
+        if ((uint64_t)p->max_blocks * KVDEC_PAGE_SIZE > 0x7fffffffull)
+            return fail(KVDEC_ERR_INVALID_ARG, "max_blocks too large");
+        cap = p->max_blocks * KVDEC_PAGE_SIZE;
+    } else {
+        if (p->capacity < 1) return fail(KVDEC_ERR_INVALID_ARG, "capacity must be >= 1");
+        rows = (uint64_t)p->batch * p->num_kv_heads * p->capacity;
+        cap = p->capacity;
+    }
+    if (rows + KVDEC_PAGE_SIZE >= 0x7fffffffull)
+        return fail(KVDEC_ERR_UNSUPPORTED, "cache has %llu rows (limit 2^31 - 64)",
+                    (unsigned long long)rows);
+    CUtensorMap tk, tv;
+    st = encode_2d(&tk, p->k, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != KVDEC_OK) return st;
+    st = encode_2d(&tv, p->v, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != KVDEC_OK) return st;
+
+    kvdec::GqaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = static_cast<const __nv_bfloat16*>(p->q);
+    a.block_table = p->block_table;
+    a.seqlens = p->seqlens;
+    a.out = p->out;
+    a.lse = p->lse;
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    a.counters = reinterpret_cast<unsigned long long*>(ws);
+    a.epoch = next_epoch();
+    a.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
+    a.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+    a.err = p->error_flag;
+    a.B = p->batch;
+    a.H = p->num_heads;
+    a.n_kv = p->num_kv_heads;
+    a.g = pl.g;
+    a.n_hc = pl.n_hc;
+    a.hc_rows = pl.hc_rows;
+    a.cap = cap;
+    a.paged = paged ? 1 : 0;
+    a.num_pages = p->num_pages;
+    a.max_blocks = p->max_blocks;
+    a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt((double)pl.D);
+    a.scale_log2 = (float)(scale * 1.4426950408889634);
+    a.min_tiles = 8;
+    a.timeout_ns = kvdec::kDefaultTimeoutNs;
+    cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, tk, tv, a, pl.grid, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
+    return KVDEC_OK;
+}
+
+kvdec_status kvdec_combine_splits(const kvdec_combine_params* p, void* stream) {
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "params is NULL");
+    if (!p->partial_o || !p->partial_lse || !p->out)
+        return fail(KVDEC_ERR_INVALID_ARG, "partial_o, partial_lse and out must be non-NULL");
+    if (p->num_splits < 1 || p->rows < 1)
+        return fail(KVDEC_ERR_INVALID_ARG, "num_splits and rows must be >= 1");
+    if (p->head_dim < 4 || p->head_dim % 4 || p->head_dim > 1024)
+        return fail(KVDEC_ERR_UNSUPPORTED, "head_dim %d (multiple of 4, <= 1024)", p->head_dim);
+    if (!aligned(p->partial_o, 16) || !aligned(p->out, 16))
+        return fail(KVDEC_ERR_INVALID_ARG, "partial_o and out must be 16-byte aligned");
+    if (p->out_dtype != KVDEC_F32 && p->out_dtype != KVDEC_BF16)
+        return fail(KVDEC_ERR_INVALID_ARG, "out_dtype %d", p->out_dtype);
+    kvdec::CombineArgs a;
+    a.po = p->partial_o;
+    a.plse = p->partial_lse;
+    a.counts = p->split_counts;
+    a.out = p->out;
+    a.lse = p->lse;
+    a.S = p->num_splits;
+    a.rows = p->rows;
+    a.D = p->head_dim;
+    a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    cudaError_t e = kvdec::launch_combine(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+    return KVDEC_OK;
+}
+
+kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "params is NULL");
+    if (p->batch < 1) return fail(KVDEC_ERR_INVALID_ARG, "batch must be >= 1");
+    if (!p->seqlens) return fail(KVDEC_ERR_INVALID_ARG, "seqlens is NULL");
+    kvdec::AppendArgs a;
+    memset(&a, 0, sizeof(a));
+    a.B = p->batch;
+    a.seqlens = p->seqlens;
+    a.block_table = p->block_table;
+    a.num_pages = p->num_pages;
+    a.max_blocks = p->max_blocks;
+    a.theta = p->rope_theta != 0.f ? (double)p->rope_theta : 10000.0;
+    a.err = p->error_flag;
+    if (p->block_table && (p->num_pages < 1 || p->max_blocks < 1))
+        return fail(KVDEC_ERR_INVALID_ARG, "paged append needs num_pages >= 1 and max_blocks >= 1");
+    if (p->mode == KVDEC_APPEND_MLA) {
+        if (!p->block_table || !p->c_kv || !p->k_rope || !p->cache)
+            return fail(KVDEC_ERR_INVALID_ARG, "MLA append needs block_table, c_kv, k_rope and cache");
+        if (!aligned(p->c_kv, 16) || !aligned(p->cache, 16) || !aligned(p->k_rope, 4))
+            return fail(KVDEC_ERR_INVALID_ARG, "c_kv and cache must be 16-byte aligned");
+        a.mode = 0;
+        a.c_kv = static_cast<const __nv_bfloat16*>(p->c_kv);
+        a.k_rope = static_cast<const __nv_bfloat16*>(p->k_rope);
+        a.cache = static_cast<__nv_bfloat16*>(p->cache);
+    } else if (p->mode == KVDEC_APPEND_GQA) {
+        if (!p->k_new || !p->v_new || !p->k || !p->v)
+            return fail(KVDEC_ERR_INVALID_ARG, "GQA append needs k_new, v_new, k and v");
+        if (p->head_dim != 64 && p->head_dim != 128)
+            return fail(KVDEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", p->head_dim);
+        if (p->num_kv_heads < 1 || p->num_kv_heads > 65535)
+            return fail(KVDEC_ERR_INVALID_ARG, "num_kv_heads %d", p->num_kv_heads);
+        if (!p->block_table && p->capacity < 1)
+            return fail(KVDEC_ERR_INVALID_ARG, "contiguous append needs capacity >= 1");
+        if (!aligned(p->v_new, 16) || !aligned(p->v, 16) || !aligned(p->k_new, 4) || !aligned(p->k, 4))
+            return fail(KVDEC_ERR_INVALID_ARG, "v_new and v must be 16-byte aligned");
+        a.mode = 1;
+        a.k_new = static_cast<const __nv_bfloat16*>(p->k_new);
+        a.v_new = static_cast<const __nv_bfloat16*>(p->v_new);
+        a.k = static_cast<__nv_bfloat16*>(p->k);
+        a.v = static_cast<__nv_bfloat16*>(p->v);
+        a.n_kv = p->num_kv_heads;
+        a.d = p->head_dim;
+        a.cap = p->capacity;
+    } else {
+        return fail(KVDEC_ERR_INVALID_ARG, "mode %d", p->mode);
+    }
+    cudaError_t e = kvdec::launch_append(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    return KVDEC_OK;
+}
+
+kvdec_status kvdec_selftest_wait_timeout(uint64_t timeout_ns, uint32_t* error_flag, void* stream) {
+    if (!error_flag) return fail(KVDEC_ERR_INVALID_ARG, "error_flag is NULL");
+    if (timeout_ns > 10000000000ull) return fail(KVDEC_ERR_INVALID_ARG, "timeout above 10 s");
+    cudaError_t e = kvdec::launch_selftest_wait(timeout_ns, error_flag, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+    return KVDEC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Cache append with RoPE: one new token per sequence ([KVC-LLM] "KV Cache
+// 如何影响了 LLM Inference" §2.2: each step appends the new k, v row;
+// [ARG] "attention-variants-and-kv-cache" §四.2: the MLA cache row is
+// [c_kv ; k_R] with k_R stored already rotated, §四.4: R_m depends only on the
+// position m).
+//
+// RoPE reading: interleaved pairs (2i, 2i+1) rotated by
+// pos * theta^(-2i/dim).  The angle reaches 1.3e5 rad at 128K context, where
+// a binary32 angle is off by ~1e-2 rad; the angle, its sine/cosine and the
+// rotation are therefore taken in binary64 and rounded once to bf16
+// (nearest-even).  The kernel moves a few KB per call: it is launch-latency
+// bound, so it is written for simplicity, one CTA per (sequence, head).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace kvdec {
+
+
+KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int dim, int pos,
+                            double theta) {
+    const double inv = pow(theta, -2.0 * (double)i / (double)dim);
+    double s, c;
+    sincos((double)pos * inv, &s, &c);
+    const double x0 = (double)__bfloat162float(x[2 * i]);
+    const double x1 = (double)__bfloat162float(x[2 * i + 1]);
+    y[2 * i] = __double2bfloat16(x0 * c - x1 * s);
+    y[2 * i + 1] = __double2bfloat16(x0 * s + x1 * c);
+}
+
+__global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
+    const int b = blockIdx.x, head = blockIdx.y, t = threadIdx.x;
+    const int pos = __ldg(a.seqlens + b);
+    const int cap = a.block_table ? a.max_blocks * KVDEC_PAGE_SIZE : a.cap;
+    if (pos < 0 || pos >= cap) {
+        if (t == 0 && head == 0) report(a.err, KVDEC_DEVERR_SEQLEN);
+        return;
+    }
+    int page = 0;
+    if (a.block_table) {
+        page = __ldg(a.block_table + (size_t)b * a.max_blocks + pos / KVDEC_PAGE_SIZE);
+        if (page < 0 || page >= a.num_pages) {
+            if (t == 0 && head == 0) report(a.err, KVDEC_DEVERR_BAD_PAGE);
+            return;
+        }
+    }
+    const int slot = pos % KVDEC_PAGE_SIZE;
+    if (a.mode == 0) {
+        // MLA latent row: [c_kv (512, copied) ; RoPE(k_rope) (64)]
+        __nv_bfloat16* row = a.cache + ((size_t)page * KVDEC_PAGE_SIZE + slot) * (KVDEC_MLA_DC + KVDEC_MLA_DR);
+        const uint4* src = reinterpret_cast<const uint4*>(a.c_kv + (size_t)b * KVDEC_MLA_DC);
+        reinterpret_cast<uint4*>(row)[t] = __ldg(src + t);     // 64 threads x 16 B = 512 bf16
+        if (t < KVDEC_MLA_DR / 2)
+            rope_pair(a.k_rope + (size_t)b * KVDEC_MLA_DR, row + KVDEC_MLA_DC, t, KVDEC_MLA_DR, pos,
+                      a.theta);
+        return;
+    }
+    // GQA: K row rotated over the whole head dim, V row copied
+    const size_t src_off = ((size_t)b * a.n_kv + head) * a.d;
+    size_t dst_off;
+    if (a.block_table) dst_off = (((size_t)page * a.n_kv + head) * KVDEC_PAGE_SIZE + slot) * a.d;
+    else dst_off = (((size_t)b * a.n_kv + head) * a.cap + pos) * a.d;
+    if (t < a.d / 2) rope_pair(a.k_new + src_off, a.k + dst_off, t, a.d, pos, a.theta);
+    if (t < a.d / 8)
+        reinterpret_cast<uint4*>(a.v + dst_off)[t] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src_off) + t);
+}
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+    dim3 grid(a.B, a.mode == 0 ? 1 : a.n_kv);
+    append_rope_kernel<<<grid, 64, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace kvdec

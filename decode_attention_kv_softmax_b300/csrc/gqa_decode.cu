@@ -1,0 +1,485 @@
+// MHA / GQA / MQA split-KV decode attention for sm_103a.
+//
+// What it computes ([ARG] "attention-variants-and-kv-cache" §二.1, §三.2;
+// [CH7] shippingwang.com ch.7 §7.3): for sequence b and query head h,
+//   out[b,h] = softmax_j(scale * q[b,h] . K[b, h/g, j]) V[b, h/g, j],
+// reading each KV head once for all g query heads of its group.
+//
+// Design (B300):
+//  * One CTA = 1 producer warp + 4 consumer warps.  The producer streams
+//    64-token K and V tiles with 2-D TMA (128-byte swizzle, L2 evict-first)
+//    into an NS-stage shared-memory ring guarded by mbarriers.
+//  * Each consumer warp takes 16 of a tile's 64 tokens and runs the whole
+//    softmax-attention step on the tensor cores with warp-level
+//    m16n8k16 bf16 MMA: S = Q K^T with the group's query heads as the 16
+//    MMA rows (zero padded; g > 16 uses two row tiles), an online softmax
+//    with quad shuffles (exp2 on the SFU), then O += P V with P taken straight
+//    from the S accumulators.  The contraction is tiny (16 x 64 x D per tile),
+//    so the kernel stays HBM-bound; the tensor cores only keep the issue
+//    slots free for the memory pipeline.
+//  * Work is split by the balanced tile schedule in schedule.cuh: every CTA
+//    streams the same number of tiles; pieces of a (b, kv head) unit that
+//    cross CTAs are merged by log-sum-exp ([ARG] §五.2) in the same kernel by
+//    the last CTA to finish the unit.
+#include "common.cuh"
+#include "kernels.h"
+#include "schedule.cuh"
+
+namespace kvdec {
+
+
+template <int D, int MT, int NS>
+struct GqaSmem {
+    static constexpr int kBoxBytes = 64 * 128;                // 64 rows x 128 B
+    static constexpr int kBoxes = D / 64;
+    static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K or V tile
+    static constexpr int kStageBytes = 2 * kTileBytes;
+    static constexpr int kRows = 16 * MT;
+    static constexpr int kOStride = D + 8;                    // padded fp32 row
+    static constexpr int kObuf = NS * kStageBytes;
+    static constexpr int kStat = kObuf + kRows * kOStride * 4;  // [4 warps][16][2]
+    static constexpr int kRowML = kStat + 4 * 16 * 2 * 4;       // [rows][2]
+    static constexpr int kBars = kRowML + kRows * 2 * 4;
+    static constexpr int kMisc = kBars + 2 * NS * 8;            // ints
+    static constexpr int kScratch = kMisc + 4 * 4;
+    static constexpr int kCum = kScratch + 160 * 4;
+    static constexpr int bytes(int B) { return kCum + (B + 1) * 4 + 1024; }
+};
+
+template <int D, int MT, int NS>
+__global__ void __launch_bounds__(160, 2)
+    gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const GqaArgs a) {
+    using L = GqaSmem<D, MT, NS>;
+    constexpr int ROWS = L::kRows;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* obuf = reinterpret_cast<float*>(smem + L::kObuf);
+    float* stat = reinterpret_cast<float*>(smem + L::kStat);
+    float* rowml = reinterpret_cast<float*>(smem + L::kRowML);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+    volatile int* misc = reinterpret_cast<volatile int*>(smem + L::kMisc);
+    int* scratch = reinterpret_cast<int*>(smem + L::kScratch);
+    int* cum = reinterpret_cast<int*>(smem + L::kCum);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t full0 = smem_addr(bars), empty0 = smem_addr(bars + NS);
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            mbar_init(empty0 + 8 * s, 4);
+        }
+        misc[0] = 0;
+        misc[1] = 0;
+        fence_barrier_init();
+    }
+    build_cum(cum, scratch, a.seqlens, a.B, a.cap, a.err);
+
+    TileSchedule S;
+    S.cum = cum;
+    S.B = a.B;
+    S.upb = a.n_kv * a.n_hc;
+    S.T = (long long)cum[a.B] * S.upb;
+    S.W = effective_items(S.T, gridDim.x, a.min_tiles);
+    const int w = blockIdx.x;
+    if (w >= S.W) return;
+    const long long t_begin = S.item_begin(w), t_end = S.item_begin(w + 1);
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        const uint64_t pol = l2_policy_evict_first();
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+        TileCursor cur;
+        if (t_begin < t_end) cur.start(S, t_begin);
+        long long issued = 0;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (long long t = t_begin; t < t_end; ++t) {
+            if (!wait_or_abort(empty0 + 8 * stage, phase ^ 1, misc, a.err, a.timeout_ns)) break;
+            const int kvh = cur.j / a.n_hc;
+            int row;
+            if (a.paged) {
+                int page = __ldg(a.block_table + (size_t)cur.b * a.max_blocks + cur.lt);
+                if (page < 0 || page >= a.num_pages) {
+                    report(a.err, KVDEC_DEVERR_BAD_PAGE);
+                    page = 0;
+                }
+                row = (page * a.n_kv + kvh) * kTileTokens;
+            } else {
+                row = (cur.b * a.n_kv + kvh) * a.cap + cur.lt * kTileTokens;
+            }
+            const uint32_t fb = full0 + 8 * stage;
+            mbar_arrive_expect_tx(fb, L::kStageBytes);
+            const uint32_t dst = smem_addr(smem + stage * L::kStageBytes);
+#pragma unroll
+            for (int x = 0; x < L::kBoxes; ++x) {
+                tma_load_2d(dst + x * L::kBoxBytes, &tmK, fb, x * 64, row, pol);
+                tma_load_2d(dst + L::kTileBytes + x * L::kBoxBytes, &tmV, fb, x * 64, row, pol);
+            }
+            ++issued;
+            if (++stage == NS) {
+                stage = 0;
+                phase ^= 1;
+            }
+            cur.advance(S);
+        }
+        // drain: never leave the CTA with TMA writes in flight
+        for (long long i = (issued > NS ? issued - NS : 0); i < issued; ++i) {
+            const int st = (int)(i % NS);
+            const uint32_t par = (uint32_t)((i / NS) & 1);
+            if (!mbar_wait_bounded(full0 + 8 * st, par, a.timeout_ns)) {
+                report(a.err, KVDEC_DEVERR_TIMEOUT);
+                break;
+            }
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    // Warp roles: warp w owns M-tile mt_w (16 head rows) and TPW tokens of
+    // every tile, so a warp's registers do not depend on the group size.
+    constexpr int WPM = 4 / MT;          // warps per M-tile
+    constexpr int TPW = 16 * MT;         // tokens per warp per tile
+    constexpr int NT = TPW / 8;          // 8-token MMA column tiles per warp
+    const int quad = lane >> 2, qc = lane & 3;
+    const int mt_w = warp / WPM;
+    const int tok_base = (warp % WPM) * TPW;
+
+    // units with no tokens: out = 0, lse = -inf (shared out round-robin)
+    for (int b = 0; b < a.B; ++b) {
+        if (S.ntiles(b) != 0) continue;
+        for (int j = 0; j < S.upb; ++j) {
+            if ((b * S.upb + j) % S.W != w) continue;
+            const int kvh = j / a.n_hc, hc = j % a.n_hc;
+            const int nr = min(a.hc_rows, a.g - hc * a.hc_rows);
+            for (int i = tid; i < nr * D; i += 128) {
+                const int r = i / D, c = i % D;
+                const size_t o = ((size_t)b * a.H + kvh * a.g + hc * a.hc_rows + r) * D + c;
+                if (a.out_bf16) reinterpret_cast<__nv_bfloat16*>(a.out)[o] = __float2bfloat16(0.f);
+                else reinterpret_cast<float*>(a.out)[o] = 0.f;
+            }
+            if (a.lse && tid < nr)
+                a.lse[(size_t)b * a.H + kvh * a.g + hc * a.hc_rows + tid] = -INFINITY;
+        }
+    }
+    if (t_begin >= t_end) return;
+
+    TileCursor cur;
+    cur.start(S, t_begin);
+    int stage = 0;
+    uint32_t phase = 0;
+
+    uint32_t qa[D / 16][4];
+    float o[D / 8][4];
+    float m[2], l[2];
+    int len = 0, nrows = 0;
+    bool seg_start = true, seg_item_first = true, seg_unit_first = true;
+    const float sl2 = a.scale_log2;
+
+    for (long long t = t_begin; t < t_end; ++t) {
+        if (seg_start) {
+            seg_start = false;
+            seg_item_first = (t == t_begin);
+            seg_unit_first = (cur.lt == 0);
+            len = clamp_len(__ldg(a.seqlens + cur.b), a.cap, nullptr);
+            const int kvh = cur.j / a.n_hc, hc = cur.j % a.n_hc;
+            nrows = min(a.hc_rows, a.g - hc * a.hc_rows);
+            const int h0 = kvh * a.g + hc * a.hc_rows;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int r = 16 * mt_w + quad + 8 * half;
+                const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                    a.q + ((size_t)cur.b * a.H + h0 + min(r, nrows - 1)) * D);
+                const bool ok = r < nrows;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    qa[ks][half] = ok ? __ldg(qrow + ks * 8 + qc) : 0u;
+                    qa[ks][half + 2] = ok ? __ldg(qrow + ks * 8 + 4 + qc) : 0u;
+                }
+            }
+            m[0] = m[1] = -INFINITY;
+            l[0] = l[1] = 0.f;
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+        }
+        const int n_valid = min(kTileTokens, len - cur.lt * kTileTokens);
+
+        if (wait_or_abort(full0 + 8 * stage, phase, misc, a.err, a.timeout_ns)) {
+            const uint32_t kb = smem_addr(smem + stage * L::kStageBytes);
+            const uint32_t vb = kb + L::kTileBytes;
+            // ---- S = Q K^T over this warp's TPW tokens
+            float s[NT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t tok = tok_base + nt * 8 + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    const uint32_t chunk = 4 * kk + (lane >> 3);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
+                    mma_bf16_16816(s[nt], qa[2 * kk], r0, r1);
+                    mma_bf16_16816(s[nt], qa[2 * kk + 1], r2, r3);
+                }
+            }
+            const bool partial = n_valid < kTileTokens;
+            if (partial) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int tk = tok_base + nt * 8 + 2 * qc;
+                    if (tk >= n_valid) s[nt][0] = s[nt][2] = -INFINITY;
+                    if (tk + 1 >= n_valid) s[nt][1] = s[nt][3] = -INFINITY;
+                }
+            }
+            // ---- online softmax (base 2, scaled) and P fragments
+            float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+                mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            const float mn0 = fmaxf(m[0], mx0 * sl2), mn1 = fmaxf(m[1], mx1 * sl2);
+            const float b0 = (mn0 == -INFINITY) ? 0.f : mn0;
+            const float b1 = (mn1 == -INFINITY) ? 0.f : mn1;
+            const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
+            m[0] = mn0;
+            m[1] = mn1;
+            float ps0 = 0.f, ps1 = 0.f;
+            uint32_t pa[MT][4];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const float p0 = fast_exp2(fmaf(s[nt][0], sl2, -b0));
+                const float p1 = fast_exp2(fmaf(s[nt][1], sl2, -b0));
+                const float p2 = fast_exp2(fmaf(s[nt][2], sl2, -b1));
+                const float p3 = fast_exp2(fmaf(s[nt][3], sl2, -b1));
+                ps0 += p0 + p1;
+                ps1 += p2 + p3;
+                pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
+                pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+            }
+            l[0] = fmaf(l[0], al0, ps0);
+            l[1] = fmaf(l[1], al1, ps1);
+#pragma unroll
+            for (int nd = 0; nd < D / 8; ++nd) {
+                o[nd][0] *= al0;
+                o[nd][1] *= al0;
+                o[nd][2] *= al1;
+                o[nd][3] *= al1;
+            }
+            // ---- O += P V, one 16-token k-step at a time
+#pragma unroll
+            for (int ks = 0; ks < MT; ++ks) {
+                const int tk = tok_base + 16 * ks + 2 * qc;
+                const uint32_t keep_lo = (tk < n_valid ? 0x0000ffffu : 0u) | (tk + 1 < n_valid ? 0xffff0000u : 0u);
+                const uint32_t keep_hi = (tk + 8 < n_valid ? 0x0000ffffu : 0u) | (tk + 9 < n_valid ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                    const int mat = lane >> 3;
+                    const uint32_t tok = tok_base + 16 * ks + (mat & 1) * 8 + (lane & 7);
+                    const uint32_t chunk = 2 * nd2 + (mat >> 1);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(vb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
+                    if (partial) {
+                        r0 &= keep_lo;
+                        r2 &= keep_lo;
+                        r1 &= keep_hi;
+                        r3 &= keep_hi;
+                    }
+                    mma_bf16_16816(o[2 * nd2], pa[ks], r0, r1);
+                    mma_bf16_16816(o[2 * nd2 + 1], pa[ks], r2, r3);
+                }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+        if (++stage == NS) {
+            stage = 0;
+            phase ^= 1;
+        }
+
+        const bool seg_end = (cur.lt == cur.nt - 1) || (t == t_end - 1);
+        if (seg_end) {
+            // ---------------------------------------------------------- flush
+            const bool unit_last = (cur.lt == cur.nt - 1);
+            const bool complete = seg_unit_first && unit_last;
+            const int kvh = cur.j / a.n_hc, hc = cur.j % a.n_hc;
+            const int h0 = kvh * a.g + hc * a.hc_rows;
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+                if (qc == 0) {
+                    stat[(warp * 16 + quad + 8 * r) * 2] = m[r];
+                    stat[(warp * 16 + quad + 8 * r) * 2 + 1] = l[r];
+                }
+            }
+            named_barrier(1, 128);
+            if (tid < ROWS) {
+                // row tid of the chunk = row (tid % 16) of M-tile tid / 16
+                const int mt = tid >> 4, lr = tid & 15;
+                float M = -INFINITY;
+                for (int ww = mt * WPM; ww < (mt + 1) * WPM; ++ww) M = fmaxf(M, stat[(ww * 16 + lr) * 2]);
+                float Lsum = 0.f;
+                if (M != -INFINITY)
+                    for (int ww = mt * WPM; ww < (mt + 1) * WPM; ++ww)
+                        Lsum += stat[(ww * 16 + lr) * 2 + 1] * fast_exp2(stat[(ww * 16 + lr) * 2] - M);
+                rowml[tid * 2] = M;
+                rowml[tid * 2 + 1] = Lsum;
+            }
+            named_barrier(1, 128);
+            for (int step = 0; step < WPM; ++step) {
+                if (warp % WPM == step) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const int row = 16 * mt_w + quad + 8 * r;
+                        const float M = rowml[row * 2];
+                        const float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
+                        float* dst = obuf + row * L::kOStride + 2 * qc;
+#pragma unroll
+                        for (int nd = 0; nd < D / 8; ++nd) {
+                            float2 v = make_float2(o[nd][2 * r] * sc, o[nd][2 * r + 1] * sc);
+                            float2* p2 = reinterpret_cast<float2*>(dst + nd * 8);
+                            if (step == 0) *p2 = v;
+                            else {
+                                float2 u = *p2;
+                                *p2 = make_float2(u.x + v.x, u.y + v.y);
+                            }
+                        }
+                    }
+                }
+                named_barrier(1, 128);
+            }
+            // normalised result rows -> final output or a partial slot
+            const int unit = cur.b * S.upb + cur.j;
+            int slot = 0;
+            if (!complete) slot = 2 * w + (seg_item_first ? 0 : 1);
+            for (int i = tid; i < nrows * (D / 4); i += 128) {
+                const int r = i / (D / 4), c4 = i % (D / 4);
+                const float Lr = rowml[r * 2 + 1];
+                const float inv = Lr > 0.f ? 1.f / Lr : 0.f;
+                float4 v = *reinterpret_cast<const float4*>(obuf + r * L::kOStride + c4 * 4);
+                v.x *= inv; v.y *= inv; v.z *= inv; v.w *= inv;
+                if (complete) {
+                    const size_t off = ((size_t)cur.b * a.H + h0 + r) * D + c4 * 4;
+                    if (a.out_bf16) {
+                        uint2 pk = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                        *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) = pk;
+                    } else {
+                        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = v;
+                    }
+                } else {
+                    *reinterpret_cast<float4*>(a.part_o + ((size_t)slot * a.hc_rows + r) * D + c4 * 4) = v;
+                }
+            }
+            if (tid < nrows) {
+                const float M = rowml[tid * 2], Lr = rowml[tid * 2 + 1];
+                const float lse_v = (Lr > 0.f) ? (M + __log2f(Lr)) * kLn2 : -INFINITY;
+                if (complete) {
+                    if (a.lse) a.lse[(size_t)cur.b * a.H + h0 + tid] = lse_v;
+                } else {
+                    a.part_lse[(size_t)slot * a.hc_rows + tid] = lse_v;
+                }
+            }
+            if (!complete) {
+                __threadfence();
+                named_barrier(1, 128);
+                if (tid == 0)
+                    misc[1] = arrive_piece(a.counters + unit, a.epoch,
+                                           (uint32_t)S.num_pieces(cur.b, cur.j)) ? 1 : 0;
+                named_barrier(1, 128);
+                if (misc[1]) {
+                    // last piece of this unit: merge every piece's partial
+                    __threadfence();
+                    const int np = S.num_pieces(cur.b, cur.j);
+                    for (int i = tid; i < nrows * (D / 4); i += 128) {
+                        const int r = i / (D / 4), c4 = i % (D / 4);
+                        float M = -INFINITY;
+                        for (int s2 = 0; s2 < np; ++s2) {
+                            const int sl = S.piece_slot(cur.b, cur.j, s2);
+                            M = fmaxf(M, __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r));
+                        }
+                        float den = 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        for (int s2 = 0; s2 < np; ++s2) {
+                            const int sl = S.piece_slot(cur.b, cur.j, s2);
+                            const float ls = __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r);
+                            const float wgt = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                            const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                a.part_o + ((size_t)sl * a.hc_rows + r) * D + c4 * 4));
+                            den += wgt;
+                            acc.x = fmaf(wgt, v.x, acc.x);
+                            acc.y = fmaf(wgt, v.y, acc.y);
+                            acc.z = fmaf(wgt, v.z, acc.z);
+                            acc.w = fmaf(wgt, v.w, acc.w);
+                        }
+                        const float inv = den > 0.f ? 1.f / den : 0.f;
+                        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+                        const size_t off = ((size_t)cur.b * a.H + h0 + r) * D + c4 * 4;
+                        if (a.out_bf16) {
+                            uint2 pk = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+                            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) = pk;
+                        } else {
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc;
+                        }
+                        if (c4 == 0 && a.lse)
+                            a.lse[(size_t)cur.b * a.H + h0 + r] =
+                                (den > 0.f) ? M + __logf(den) : -INFINITY;
+                    }
+                    if (tid == 0) a.counters[unit] = 0ull;
+                }
+            }
+            named_barrier(1, 128);
+            seg_start = true;
+        }
+        cur.advance(S);
+    }
+}
+
+// ---------------------------------------------------------------- launcher
+
+template <int D, int MT, int NS>
+static cudaError_t launch_gqa_t(const CUtensorMap& tk, const CUtensorMap& tv, const GqaArgs& a,
+                                int grid, cudaStream_t st) {
+    using L = GqaSmem<D, MT, NS>;
+    const int smem = L::bytes(a.B);
+    auto kern = gqa_decode_kernel<D, MT, NS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, 160, smem, st>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
+template <int D, int MT, int NS>
+static int occupancy_gqa_t(int B) {
+    using L = GqaSmem<D, MT, NS>;
+    const int smem = L::bytes(B);
+    auto kern = gqa_decode_kernel<D, MT, NS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+        return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 160, smem) != cudaSuccess) return 0;
+    return n;
+}
+
+// Stages per configuration: a 64-token K+V tile is 32 KB at D=128, 16 KB at
+// D=64; three (six) of them keep ~96 KB in flight per CTA, two CTAs per SM.
+#define KVDEC_GQA_DISPATCH(FN, ...)                                        \
+    (D == 128 ? (MT == 1 ? FN<128, 1, 3>(__VA_ARGS__) : FN<128, 2, 3>(__VA_ARGS__)) \
+              : (MT == 1 ? FN<64, 1, 6>(__VA_ARGS__) : FN<64, 2, 6>(__VA_ARGS__)))
+
+cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const GqaArgs& a, int grid, cudaStream_t st) {
+    return KVDEC_GQA_DISPATCH(launch_gqa_t, tk, tv, a, grid, st);
+}
+
+int occupancy_gqa(int D, int MT, int B) { return KVDEC_GQA_DISPATCH(occupancy_gqa_t, B); }
+
+}  // namespace kvdec

@@ -1,0 +1,64 @@
+// Argument blocks and launchers shared between the host API (api.cu) and
+// the kernel translation units.
+#pragma once
+
+#include "common.cuh"
+
+namespace kvdec {
+
+struct GqaArgs {
+    const __nv_bfloat16* q;
+    const int32_t* block_table;
+    const int32_t* seqlens;
+    void* out;
+    float* lse;
+    float* part_o;       // [2*grid, rows, D]
+    float* part_lse;     // [2*grid, rows]
+    unsigned long long* counters;  // [units], see arrive_piece
+    uint32_t epoch;
+    uint32_t* err;
+    int B, H, n_kv, g, n_hc, hc_rows;
+    int cap;             // tokens addressable per sequence
+    int paged, num_pages, max_blocks;
+    int out_bf16;
+    float scale_log2;
+    int min_tiles;
+    uint64_t timeout_ns;
+};
+
+struct CombineArgs {
+    const float* po;
+    const float* plse;
+    const int32_t* counts;
+    void* out;
+    float* lse;
+    int S, rows, D;
+    int out_bf16;
+};
+
+struct AppendArgs {
+    int mode;  // 0 MLA, 1 GQA
+    int B;
+    const int32_t* seqlens;
+    const int32_t* block_table;
+    int num_pages, max_blocks;
+    double theta;
+    const __nv_bfloat16* c_kv;
+    const __nv_bfloat16* k_rope;
+    __nv_bfloat16* cache;
+    const __nv_bfloat16* k_new;
+    const __nv_bfloat16* v_new;
+    __nv_bfloat16* k;
+    __nv_bfloat16* v;
+    int n_kv, d, cap;
+    uint32_t* err;
+};
+
+cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,
+                       const GqaArgs& a, int grid, cudaStream_t st);
+int occupancy_gqa(int D, int MT, int B);
+cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
+cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* err, cudaStream_t st);
+
+}  // namespace kvdec

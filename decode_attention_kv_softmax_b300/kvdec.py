@@ -1,0 +1,381 @@
+"""Python binding of libkvdec (the C ABI in include/kvdec.h).
+
+Argument marshalling only: every operation runs in the library's CUDA
+kernels.  PyTorch supplies device memory and the current stream.  There is no
+fallback: if libkvdec.so is missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from ctypes import c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvdec.so")
+
+F32, BF16 = 0, 1
+APPEND_MLA, APPEND_GQA = 0, 1
+DEVERR_BAD_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
+          4: "workspace too small"}
+
+
+class GqaParams(ctypes.Structure):
+    _fields_ = [("q", c_void_p), ("k", c_void_p), ("v", c_void_p),
+                ("block_table", c_void_p), ("seqlens", c_void_p),
+                ("batch", c_int32), ("num_heads", c_int32), ("num_kv_heads", c_int32),
+                ("head_dim", c_int32), ("capacity", c_int32), ("num_pages", c_int32),
+                ("max_blocks", c_int32), ("scale", c_float), ("out", c_void_p),
+                ("out_dtype", c_int32), ("lse", c_void_p), ("workspace", c_void_p),
+                ("workspace_bytes", c_size_t), ("error_flag", c_void_p),
+                ("max_ctas", c_int32), ("reserved", c_int32)]
+
+
+class MlaParams(ctypes.Structure):
+    _fields_ = [("q_absorbed", c_void_p), ("q_rope", c_void_p), ("cache", c_void_p),
+                ("block_table", c_void_p), ("seqlens", c_void_p), ("batch", c_int32),
+                ("num_heads", c_int32), ("num_pages", c_int32), ("max_blocks", c_int32),
+                ("scale", c_float), ("out", c_void_p), ("out_dtype", c_int32),
+                ("lse", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+                ("error_flag", c_void_p), ("max_ctas", c_int32), ("reserved", c_int32)]
+
+
+class AppendParams(ctypes.Structure):
+    _fields_ = [("mode", c_int32), ("batch", c_int32), ("seqlens", c_void_p),
+                ("block_table", c_void_p), ("num_pages", c_int32), ("max_blocks", c_int32),
+                ("rope_theta", c_float), ("c_kv", c_void_p), ("k_rope", c_void_p),
+                ("cache", c_void_p), ("k_new", c_void_p), ("v_new", c_void_p),
+                ("k", c_void_p), ("v", c_void_p), ("num_kv_heads", c_int32),
+                ("head_dim", c_int32), ("capacity", c_int32), ("reserved", c_int32),
+                ("error_flag", c_void_p)]
+
+
+class CombineParams(ctypes.Structure):
+    _fields_ = [("partial_o", c_void_p), ("partial_lse", c_void_p),
+                ("split_counts", c_void_p), ("num_splits", c_int32), ("rows", c_int32),
+                ("head_dim", c_int32), ("out_dtype", c_int32), ("out", c_void_p),
+                ("lse", c_void_p)]
+
+
+EXPORTS = ["kvdec_abi_version", "kvdec_params_size", "kvdec_status_string",
+           "kvdec_last_error", "kvdec_gqa_workspace_bytes", "kvdec_gqa_decode",
+           "kvdec_mla_workspace_bytes", "kvdec_mla_decode_absorbed", "kvdec_append_rope",
+           "kvdec_combine_splits", "kvdec_selftest_wait_timeout"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: str = LIB_PATH):
+    """Load libkvdec.so (once) and check the struct layouts against it."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with "
+                "`python -m decode_attention_kv_softmax_b300.build` (no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        lib.kvdec_abi_version.restype = ctypes.c_int
+        lib.kvdec_params_size.restype = c_int64
+        lib.kvdec_params_size.argtypes = [ctypes.c_int]
+        lib.kvdec_status_string.restype = ctypes.c_char_p
+        lib.kvdec_status_string.argtypes = [ctypes.c_int]
+        lib.kvdec_last_error.restype = ctypes.c_char_p
+        for name, st in [("gqa", GqaParams), ("mla", MlaParams)]:
+            f = getattr(lib, f"kvdec_{name}_workspace_bytes")
+            f.restype = c_size_t
+            f.argtypes = [ctypes.POINTER(st)]
+        for name, st in [("kvdec_gqa_decode", GqaParams), ("kvdec_mla_decode_absorbed", MlaParams),
+                         ("kvdec_append_rope", AppendParams),
+                         ("kvdec_combine_splits", CombineParams)]:
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.POINTER(st), c_void_p]
+        lib.kvdec_selftest_wait_timeout.restype = ctypes.c_int
+        lib.kvdec_selftest_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
+        if lib.kvdec_abi_version() != 1:
+            raise RuntimeError("libkvdec ABI version mismatch")
+        for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams]):
+            if lib.kvdec_params_size(kind) != ctypes.sizeof(st):
+                raise RuntimeError(f"params struct {st.__name__} layout mismatch")
+        _lib = lib
+        return lib
+
+
+class KvdecError(RuntimeError):
+    pass
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        msg = _lib.kvdec_last_error().decode(errors="replace")
+        raise KvdecError(f"{what}: {STATUS.get(status, status)}: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(dt):
+    if dt == torch.float32:
+        return F32
+    if dt == torch.bfloat16:
+        return BF16
+    raise ValueError(f"output dtype {dt} (float32 or bfloat16)")
+
+
+def _need(t, name, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+# ---------------------------------------------------------------- workspace
+
+class Workspace:
+    """A device buffer reused across calls (grown on demand).  The library
+    needs no initialisation of it: split counters carry a per-call epoch."""
+
+    def __init__(self):
+        self._bufs = {}
+
+    def get(self, device, nbytes: int) -> torch.Tensor:
+        key = (device.index if device.index is not None else torch.cuda.current_device())
+        buf = self._bufs.get(key)
+        if buf is None or buf.numel() < nbytes:
+            buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self._bufs[key] = buf
+        return buf
+
+    def reset(self):
+        for b in self._bufs.values():
+            b.zero_()
+
+
+_default_ws = Workspace()
+
+
+def default_workspace() -> Workspace:
+    return _default_ws
+
+
+def new_error_flag(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+# ---------------------------------------------------------------- GQA
+
+def gqa_params(q, k, v, seqlens, block_table=None, scale=None, out=None, lse=None,
+               error_flag=None, max_ctas=0, workspace=None):
+    p = GqaParams()
+    B, H, D = q.shape
+    p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
+    p.block_table = _ptr(block_table)
+    p.seqlens = _ptr(seqlens)
+    p.batch, p.num_heads, p.head_dim = B, H, D
+    p.num_kv_heads = k.shape[1]
+    if block_table is None:
+        p.capacity = k.shape[2]
+    else:
+        p.num_pages = k.shape[0]
+        p.max_blocks = block_table.shape[1]
+    p.scale = float(scale) if scale else 0.0
+    p.out = _ptr(out)
+    p.out_dtype = _dtype_code(out.dtype) if out is not None else F32
+    p.lse = _ptr(lse)
+    p.error_flag = _ptr(error_flag)
+    p.max_ctas = int(max_ctas)
+    if workspace is not None:
+        p.workspace = _ptr(workspace)
+        p.workspace_bytes = workspace.numel() * workspace.element_size()
+    return p
+
+
+def gqa_workspace_bytes(q, k, v, seqlens, block_table=None, max_ctas=0) -> int:
+    lib = load()
+    p = gqa_params(q, k, v, seqlens, block_table, max_ctas=max_ctas)
+    n = lib.kvdec_gqa_workspace_bytes(ctypes.byref(p))
+    if n == 0:
+        raise KvdecError("kvdec_gqa_workspace_bytes: " + lib.kvdec_last_error().decode())
+    return n
+
+
+def gqa_decode(q, k, v, seqlens, block_table=None, scale=None, out_dtype=torch.float32,
+               out=None, return_lse=True, error_flag=None, max_ctas=0, workspace=None,
+               stream=None):
+    """MHA/GQA/MQA decode.  q [B,h,d] bf16; k, v contiguous [B,n_kv,cap,d] or
+    paged [pages,n_kv,64,d] bf16 (with block_table [B,max_blocks] int32);
+    seqlens [B] int32.  Returns (out [B,h,d], lse [B,h] or None)."""
+    lib = load()
+    dev = q.device
+    for t, n in [(q, "q"), (k, "k"), (v, "v")]:
+        _need(t, n, torch.bfloat16, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, dev)
+    if k.shape != v.shape:
+        raise ValueError("k and v must have the same shape")
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
+    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas)
+    need = lib.kvdec_gqa_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        raise KvdecError("kvdec_gqa_decode: " + lib.kvdec_last_error().decode())
+    if workspace is None:
+        workspace = _default_ws.get(dev, need)
+    p.workspace = _ptr(workspace)
+    p.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.kvdec_gqa_decode(ctypes.byref(p), _stream(stream)), "kvdec_gqa_decode")
+    return out, lse
+
+
+# ---------------------------------------------------------------- MLA
+
+def mla_params(q_abs, q_rope, cache, block_table, seqlens, scale=None, out=None, lse=None,
+               error_flag=None, max_ctas=0):
+    p = MlaParams()
+    B, H, _ = q_abs.shape
+    p.q_absorbed, p.q_rope, p.cache = _ptr(q_abs), _ptr(q_rope), _ptr(cache)
+    p.block_table, p.seqlens = _ptr(block_table), _ptr(seqlens)
+    p.batch, p.num_heads = B, H
+    p.num_pages, p.max_blocks = cache.shape[0], block_table.shape[1]
+    p.scale = float(scale) if scale else 0.0
+    p.out = _ptr(out)
+    p.out_dtype = _dtype_code(out.dtype) if out is not None else F32
+    p.lse = _ptr(lse)
+    p.error_flag = _ptr(error_flag)
+    p.max_ctas = int(max_ctas)
+    return p
+
+
+def mla_decode_absorbed(q_abs, q_rope, cache, block_table, seqlens, scale=None,
+                        out_dtype=torch.float32, out=None, return_lse=True, error_flag=None,
+                        max_ctas=0, workspace=None, stream=None):
+    """MLA absorbed decode.  q_abs [B,128,512], q_rope [B,128,64], cache
+    [pages,64,576] (all bf16); block_table [B,max_blocks] and seqlens [B]
+    int32.  Returns (out [B,128,512] latent, lse [B,128] or None)."""
+    lib = load()
+    dev = q_abs.device
+    for t, n in [(q_abs, "q_abs"), (q_rope, "q_rope"), (cache, "cache")]:
+        _need(t, n, torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    if out is None:
+        out = torch.empty(q_abs.shape, dtype=out_dtype, device=dev)
+    lse = torch.empty(q_abs.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
+    p = mla_params(q_abs, q_rope, cache, block_table, seqlens, scale, out, lse, error_flag, max_ctas)
+    need = lib.kvdec_mla_workspace_bytes(ctypes.byref(p))
+    if need == 0:
+        raise KvdecError("kvdec_mla_decode_absorbed: " + lib.kvdec_last_error().decode())
+    if workspace is None:
+        workspace = _default_ws.get(dev, need)
+    p.workspace = _ptr(workspace)
+    p.workspace_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.kvdec_mla_decode_absorbed(ctypes.byref(p), _stream(stream)),
+           "kvdec_mla_decode_absorbed")
+    return out, lse
+
+
+# ---------------------------------------------------------------- append
+
+def append_rope_mla(cache, block_table, seqlens, c_kv, k_rope, rope_theta=10000.0,
+                    error_flag=None, stream=None):
+    """Write [c_kv ; RoPE_pos(k_rope)] at slot seqlens[b] of the paged latent
+    cache (in place).  The caller increments seqlens afterwards."""
+    lib = load()
+    dev = cache.device
+    for t, n in [(cache, "cache"), (c_kv, "c_kv"), (k_rope, "k_rope")]:
+        _need(t, n, torch.bfloat16, dev)
+    _need(block_table, "block_table", torch.int32, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    p = AppendParams()
+    p.mode = APPEND_MLA
+    p.batch = c_kv.shape[0]
+    p.seqlens, p.block_table = _ptr(seqlens), _ptr(block_table)
+    p.num_pages, p.max_blocks = cache.shape[0], block_table.shape[1]
+    p.rope_theta = rope_theta
+    p.c_kv, p.k_rope, p.cache = _ptr(c_kv), _ptr(k_rope), _ptr(cache)
+    p.error_flag = _ptr(error_flag)
+    _check(lib.kvdec_append_rope(ctypes.byref(p), _stream(stream)), "kvdec_append_rope")
+
+
+def append_rope_gqa(k, v, seqlens, k_new, v_new, block_table=None, rope_theta=10000.0,
+                    error_flag=None, stream=None):
+    """K[.., pos, :] = RoPE_pos(k_new), V[.., pos, :] = v_new at pos =
+    seqlens[b] (in place), contiguous or paged caches."""
+    lib = load()
+    dev = k.device
+    for t, n in [(k, "k"), (v, "v"), (k_new, "k_new"), (v_new, "v_new")]:
+        _need(t, n, torch.bfloat16, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    p = AppendParams()
+    p.mode = APPEND_GQA
+    p.batch = k_new.shape[0]
+    p.seqlens = _ptr(seqlens)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, dev)
+        p.block_table = _ptr(block_table)
+        p.num_pages, p.max_blocks = k.shape[0], block_table.shape[1]
+    else:
+        p.capacity = k.shape[2]
+    p.rope_theta = rope_theta
+    p.k_new, p.v_new, p.k, p.v = _ptr(k_new), _ptr(v_new), _ptr(k), _ptr(v)
+    p.num_kv_heads, p.head_dim = k_new.shape[1], k_new.shape[2]
+    p.error_flag = _ptr(error_flag)
+    _check(lib.kvdec_append_rope(ctypes.byref(p), _stream(stream)), "kvdec_append_rope")
+
+
+# ---------------------------------------------------------------- combine
+
+def combine_splits(partial_o, partial_lse, split_counts=None, out_dtype=torch.float32,
+                   out=None, return_lse=True, stream=None):
+    """partial_o [S, R, D] fp32 (normalised), partial_lse [S, R] fp32,
+    split_counts [R] int32 or None.  Returns (out [R, D], lse [R])."""
+    lib = load()
+    dev = partial_o.device
+    _need(partial_o, "partial_o", torch.float32, dev)
+    _need(partial_lse, "partial_lse", torch.float32, dev)
+    S, R, D = partial_o.shape
+    if split_counts is not None:
+        _need(split_counts, "split_counts", torch.int32, dev)
+    if out is None:
+        out = torch.empty((R, D), dtype=out_dtype, device=dev)
+    lse = torch.empty(R, dtype=torch.float32, device=dev) if return_lse else None
+    p = CombineParams()
+    p.partial_o, p.partial_lse = _ptr(partial_o), _ptr(partial_lse)
+    p.split_counts = _ptr(split_counts)
+    p.num_splits, p.rows, p.head_dim = S, R, D
+    p.out_dtype = _dtype_code(out.dtype)
+    p.out, p.lse = _ptr(out), _ptr(lse)
+    _check(lib.kvdec_combine_splits(ctypes.byref(p), _stream(stream)), "kvdec_combine_splits")
+    return out, lse
+
+
+def selftest_wait_timeout(timeout_ns: int, error_flag, stream=None):
+    lib = load()
+    _check(lib.kvdec_selftest_wait_timeout(timeout_ns, _ptr(error_flag), _stream(stream)),
+           "kvdec_selftest_wait_timeout")
+
+
+def default_scale_gqa(d: int) -> float:
+    return 1.0 / math.sqrt(d)

@@ -1,0 +1,276 @@
+/*
+ * kvdec.h -- C ABI of libkvdec: single-token decode attention over a KV cache
+ * on NVIDIA B300 (sm_103a).
+ *
+ * Four operations (plus helpers):
+ *   kvdec_gqa_decode           MHA / GQA / MQA split-KV decode
+ *   kvdec_mla_decode_absorbed  MLA decode over the 576-wide latent cache
+ *   kvdec_append_rope          write one new token per sequence into a cache
+ *   kvdec_combine_splits       log-sum-exp merge of split partial outputs
+ *
+ * Sources, cited by page title and section:
+ *   [KVC-LLM] "KV Cache 如何影响了 LLM Inference" (kakack.github.io)
+ *   [ARG]     "attention-variants-and-kv-cache" (arganzheng.life)
+ *   [MLA]     "multi-head-latent-attention" (jianzhnie.github.io)
+ *   [AIFAQ]   aifaq.phimes.top (decoupled-RoPE Q&A)
+ *   [CH7]     shippingwang.com ch.7 "KV Cache 优化"
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller, dense
+ *     row-major in the stated shape.  bf16 is IEEE-style bfloat16.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream) and allocates nothing.
+ *   - Host-side argument checks run before any launch; a failed check returns
+ *     an error status and launches nothing.  C++ exceptions never cross the
+ *     ABI.  kvdec_last_error() gives a human-readable reason (per thread).
+ *   - Device-side problems (a block-table entry outside [0, num_pages), a
+ *     sequence length outside [0, capacity], a bounded wait that ran out) do
+ *     not fault or trap: kernels keep every access in bounds, OR a
+ *     KVDEC_DEVERR_* bit into *error_flag (when error_flag is not NULL) and
+ *     the affected outputs are unspecified.  The caller reads the word after
+ *     synchronising.
+ *   - Calls that share a workspace or an output buffer must not overlap on
+ *     the GPU.
+ */
+#ifndef KVDEC_H
+#define KVDEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVDEC_ABI_VERSION 1
+#define KVDEC_PAGE_SIZE 64      /* tokens per KV page (block) */
+#define KVDEC_MLA_DC 512        /* MLA latent width d_c */
+#define KVDEC_MLA_DR 64         /* MLA decoupled rope key width d_h^R */
+
+typedef enum kvdec_status {
+    KVDEC_OK = 0,
+    KVDEC_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misalignment */
+    KVDEC_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head_dim 96) */
+    KVDEC_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed */
+    KVDEC_ERR_WORKSPACE = 4      /* workspace missing or too small */
+} kvdec_status;
+
+/* bits OR-ed into *error_flag by the kernels */
+#define KVDEC_DEVERR_BAD_PAGE 0x1u   /* block-table entry outside [0, num_pages) */
+#define KVDEC_DEVERR_SEQLEN 0x2u     /* seqlen < 0 or > capacity (clamped) */
+#define KVDEC_DEVERR_TIMEOUT 0x4u    /* a bounded device wait ran out */
+
+typedef enum kvdec_dtype { KVDEC_F32 = 0, KVDEC_BF16 = 1 } kvdec_dtype;
+
+/* ------------------------------------------------------------------------ */
+/* MHA / GQA / MQA decode                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * For every sequence b and query head h (g = num_heads / num_kv_heads):
+ *   s_j  = scale * q[b,h,:] . K[b, h/g, j, :]            for j < seqlens[b]
+ *   out[b,h,:] = sum_j softmax(s)_j V[b, h/g, j, :],   lse[b,h] = ln sum_j e^{s_j}
+ * ([ARG] §二.1 decode attention, §三.2 grouping; [CH7] §7.3: query head h
+ * reads KV head h // g and KV is never replicated; [KVC-LLM] §2.2).
+ * The sequence is split across CTAs and the pieces merged by their
+ * log-sum-exp ([ARG] §五.2, flash-decoding); the result does not depend on
+ * the split.  seqlens[b] == 0 gives out = 0, lse = -inf.
+ *
+ * Layouts
+ *   q      bf16 [batch, num_heads, head_dim]
+ *   k, v   block_table == NULL: bf16 [batch, num_kv_heads, capacity, head_dim]
+ *          else paged:          bf16 [num_pages, num_kv_heads, 64, head_dim];
+ *          token j of sequence b lives in page block_table[b, j/64], row j%64
+ *          ([ARG] §六.1).  Pages may be shared between sequences.
+ *   block_table int32 [batch, max_blocks] (paged only)
+ *   seqlens int32 [batch]
+ *   out    [batch, num_heads, head_dim], F32 or BF16 (out_dtype)
+ *   lse    fp32 [batch, num_heads] or NULL
+ * Supported: head_dim in {64, 128}; num_heads % num_kv_heads == 0;
+ * q, k, v, out 16-byte aligned.  scale == 0 selects 1/sqrt(head_dim).
+ * Workspace: at least kvdec_gqa_workspace_bytes(p) bytes, 256-byte aligned,
+ * no initialisation needed (split counters are tagged with a per-call epoch).
+ * It holds the split partials and their counters; calls that share it must
+ * not overlap on the GPU.
+ */
+typedef struct kvdec_gqa_params {
+    const void* q;
+    const void* k;
+    const void* v;
+    const int32_t* block_table;
+    const int32_t* seqlens;
+    int32_t batch;
+    int32_t num_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;        /* contiguous: cached tokens per (b, kv head) */
+    int32_t num_pages;       /* paged only */
+    int32_t max_blocks;      /* paged only */
+    float scale;
+    void* out;
+    int32_t out_dtype;       /* kvdec_dtype */
+    float* lse;
+    void* workspace;
+    size_t workspace_bytes;
+    uint32_t* error_flag;    /* optional */
+    int32_t max_ctas;        /* 0 = one full wave of resident CTAs */
+    int32_t reserved;
+} kvdec_gqa_params;
+
+size_t kvdec_gqa_workspace_bytes(const kvdec_gqa_params* p);
+kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* MLA absorbed decode                                                       */
+/* ------------------------------------------------------------------------ */
+/*
+ * DeepSeek-style MLA after matrix absorption ([ARG] §四.5; [MLA] §4;
+ * [AIFAQ]): every cached token stores one 576-value row
+ * [c_kv (512) ; k_R (64, already rotated)] shared by all heads.  For each
+ * sequence b and head h:
+ *   s_j  = scale * (q_absorbed[b,h,:] . c_kv_j + q_rope[b,h,:] . k_R_j)
+ *   out[b,h,:] = sum_j softmax(s)_j c_kv_j        (latent space, 512 wide)
+ * V is the first 512 values of the same row.  scale == 0 selects
+ * 1/sqrt(128 + 64) = 1/sqrt(192), the pre-absorption head dim.
+ * W_UK (folded into q_absorbed) and W_UV / W_O (applied to out) are the
+ * caller's.
+ *
+ * Layouts
+ *   q_absorbed bf16 [batch, num_heads, 512]; q_rope bf16 [batch, num_heads, 64]
+ *   cache bf16 [num_pages, 64, 576]; block_table int32 [batch, max_blocks]
+ *   seqlens int32 [batch]; out [batch, num_heads, 512] F32 or BF16;
+ *   lse fp32 [batch, num_heads] or NULL
+ * Supported: num_heads == 128 (tensor-core tile height).
+ * Workspace: as for kvdec_gqa_decode (no initialisation needed).
+ */
+typedef struct kvdec_mla_params {
+    const void* q_absorbed;
+    const void* q_rope;
+    const void* cache;
+    const int32_t* block_table;
+    const int32_t* seqlens;
+    int32_t batch;
+    int32_t num_heads;
+    int32_t num_pages;
+    int32_t max_blocks;
+    float scale;
+    void* out;
+    int32_t out_dtype;
+    float* lse;
+    void* workspace;
+    size_t workspace_bytes;
+    uint32_t* error_flag;
+    int32_t max_ctas;        /* 0 = one full wave of CTA pairs */
+    int32_t reserved;
+} kvdec_mla_params;
+
+size_t kvdec_mla_workspace_bytes(const kvdec_mla_params* p);
+kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Cache append with RoPE                                                    */
+/* ------------------------------------------------------------------------ */
+/*
+ * Writes one new token per sequence at slot pos = seqlens[b] (0-based; the
+ * caller increments seqlens afterwards) -- the cache only grows by one row
+ * per decode step ([KVC-LLM] §2.2; [ARG] §二.2).  RoPE rotates interleaved
+ * pairs (2i, 2i+1) by pos * rope_theta^(-2i/dim) ([ARG] §四.4: R_m depends
+ * only on the position; the pairing and frequencies are this library's
+ * reading).  Rotated values are rounded to bf16 (nearest-even); copied values
+ * are bit-exact.
+ *
+ * mode KVDEC_APPEND_MLA ([ARG] §四.2: c_kv cached as is, k_R cached rotated):
+ *   c_kv bf16 [batch, 512], k_rope bf16 [batch, 64] (un-rotated)
+ *   -> cache bf16 [num_pages, 64, 576] row (block_table[b, pos/64], pos%64)
+ *      = [c_kv ; RoPE_pos(k_rope)]
+ * mode KVDEC_APPEND_GQA:
+ *   k_new, v_new bf16 [batch, num_kv_heads, head_dim]
+ *   -> K[.., pos, :] = RoPE_pos(k_new) (all head_dim values rotated),
+ *      V[.., pos, :] = v_new, contiguous (block_table NULL) or paged layout
+ *      exactly as in kvdec_gqa_decode.
+ * pos outside [0, capacity) or a bad page entry sets the error bit and the
+ * row is skipped.
+ */
+typedef enum kvdec_append_mode { KVDEC_APPEND_MLA = 0, KVDEC_APPEND_GQA = 1 } kvdec_append_mode;
+
+typedef struct kvdec_append_params {
+    int32_t mode;
+    int32_t batch;
+    const int32_t* seqlens;
+    const int32_t* block_table;  /* MLA: required; GQA: NULL = contiguous */
+    int32_t num_pages;
+    int32_t max_blocks;
+    float rope_theta;            /* 0 selects 10000 */
+    /* MLA */
+    const void* c_kv;
+    const void* k_rope;
+    void* cache;
+    /* GQA */
+    const void* k_new;
+    const void* v_new;
+    void* k;
+    void* v;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t capacity;            /* GQA contiguous */
+    int32_t reserved;
+    uint32_t* error_flag;        /* optional */
+} kvdec_append_params;
+
+kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Split combine                                                             */
+/* ------------------------------------------------------------------------ */
+/*
+ * Merges normalised split partials of rows = batch * num_heads rows
+ * ([ARG] §五.2, last paragraph: softmax each piece locally, then merge the
+ * normalisers).  For row r with n = split_counts[r] (or num_splits):
+ *   M = max_s lse_s,  w_s = e^{lse_s - M},
+ *   out[r,:] = sum_s w_s O_s[r,:] / sum_s w_s,   lse[r] = M + ln sum_s w_s
+ * Partials with lse = -inf (empty pieces) weigh 0; a row whose partials are
+ * all empty gets out = 0, lse = -inf; a row with split_counts[r] == 0 is left
+ * untouched.
+ *
+ * Layouts
+ *   partial_o   fp32 [num_splits, rows, head_dim]   (O_s = o_s / l_s)
+ *   partial_lse fp32 [num_splits, rows]             (natural log)
+ *   split_counts int32 [rows] or NULL (all rows use num_splits)
+ *   out [rows, head_dim] F32 or BF16; lse fp32 [rows] or NULL
+ * Supported: head_dim a multiple of 4 and <= 1024; partial_o and out
+ * 16-byte aligned.
+ */
+typedef struct kvdec_combine_params {
+    const float* partial_o;
+    const float* partial_lse;
+    const int32_t* split_counts;
+    int32_t num_splits;
+    int32_t rows;
+    int32_t head_dim;
+    int32_t out_dtype;
+    void* out;
+    float* lse;
+} kvdec_combine_params;
+
+kvdec_status kvdec_combine_splits(const kvdec_combine_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* helpers                                                                   */
+/* ------------------------------------------------------------------------ */
+int kvdec_abi_version(void);
+/* sizeof() of each params struct, so a binding can check its mirror:
+ * kind 0 gqa, 1 mla, 2 append, 3 combine; -1 for an unknown kind. */
+int64_t kvdec_params_size(int kind);
+const char* kvdec_status_string(kvdec_status s);
+const char* kvdec_last_error(void);
+/* Self-test of the bounded device wait: one CTA waits on a barrier that
+ * nothing completes, gives up after about timeout_ns nanoseconds, ORs
+ * KVDEC_DEVERR_TIMEOUT into *error_flag (device) and returns.  Lets a test
+ * check the timeout path without hanging the GPU. */
+kvdec_status kvdec_selftest_wait_timeout(uint64_t timeout_ns, uint32_t* error_flag,
+                                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVDEC_H */

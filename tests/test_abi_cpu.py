@@ -1,0 +1,70 @@
+"""The C-ABI library loads, exports every function include/kvdec.h declares,
+and agrees with the binding's struct mirrors.  Host-side argument checks are
+exercised on calls that are rejected before any CUDA work (no GPU here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from decode_attention_kv_softmax_b300 import build, kvdec
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return kvdec.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "kvdec.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvdec_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 11
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(kvdec.EXPORTS)
+
+
+def test_struct_layouts(lib):
+    assert lib.kvdec_abi_version() == 1
+    for kind, st in enumerate([kvdec.GqaParams, kvdec.MlaParams, kvdec.AppendParams,
+                               kvdec.CombineParams]):
+        assert lib.kvdec_params_size(kind) == ctypes.sizeof(st)
+    assert lib.kvdec_params_size(99) == -1
+
+
+def test_status_strings(lib):
+    for s, txt in kvdec.STATUS.items():
+        assert lib.kvdec_status_string(s).decode() == txt
+
+
+def test_host_argument_checks(lib):
+    # rejected before touching the device
+    assert lib.kvdec_gqa_decode(None, None) == 1
+    p = kvdec.GqaParams()
+    p.batch, p.num_heads, p.num_kv_heads, p.head_dim = 2, 8, 3, 128
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 1
+    assert "multiple" in lib.kvdec_last_error().decode()
+    p.num_kv_heads, p.head_dim = 2, 96
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 2
+    assert lib.kvdec_gqa_workspace_bytes(ctypes.byref(p)) == 0
+    p.head_dim, p.batch = 128, 0
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 1
+    c = kvdec.CombineParams()
+    assert lib.kvdec_combine_splits(ctypes.byref(c), None) == 1
+    a = kvdec.AppendParams()
+    a.batch = 1
+    assert lib.kvdec_append_rope(ctypes.byref(a), None) == 1
+    a.mode = 7
+    a.seqlens = 16
+    assert lib.kvdec_append_rope(ctypes.byref(a), None) == 1
+    m = kvdec.MlaParams()
+    assert lib.kvdec_mla_decode_absorbed(ctypes.byref(m), None) != 0
+    assert lib.kvdec_selftest_wait_timeout(1000, None, None) == 1

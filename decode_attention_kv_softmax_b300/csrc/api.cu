@@ -156,6 +156,11 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
 
 }  // namespace
 
+namespace kvdec {
+// Lets other translation units of the library set the kvdec_last_error text.
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace kvdec
+
 extern "C" {
 
 int kvdec_abi_version(void) { return KVDEC_ABI_VERSION; }

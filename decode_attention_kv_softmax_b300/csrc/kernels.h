@@ -60,5 +60,6 @@ int occupancy_gqa(int D, int MT, int B);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* err, cudaStream_t st);
+void set_last_error(const char* msg);
 
 }  // namespace kvdec

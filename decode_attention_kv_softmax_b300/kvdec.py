@@ -64,7 +64,8 @@ class CombineParams(ctypes.Structure):
 EXPORTS = ["kvdec_abi_version", "kvdec_params_size", "kvdec_status_string",
            "kvdec_last_error", "kvdec_gqa_workspace_bytes", "kvdec_gqa_decode",
            "kvdec_mla_workspace_bytes", "kvdec_mla_decode_absorbed", "kvdec_append_rope",
-           "kvdec_combine_splits", "kvdec_selftest_wait_timeout"]
+           "kvdec_combine_splits", "kvdec_selftest_wait_timeout",
+           "kvdec_gqa_decode_noalloc"]
 
 _lib = None
 _lock = threading.Lock()
@@ -91,7 +92,8 @@ def load(path: str = LIB_PATH):
             f = getattr(lib, f"kvdec_{name}_workspace_bytes")
             f.restype = c_size_t
             f.argtypes = [ctypes.POINTER(st)]
-        for name, st in [("kvdec_gqa_decode", GqaParams), ("kvdec_mla_decode_absorbed", MlaParams),
+        for name, st in [("kvdec_gqa_decode", GqaParams), ("kvdec_gqa_decode_noalloc", GqaParams),
+                         ("kvdec_mla_decode_absorbed", MlaParams),
                          ("kvdec_append_rope", AppendParams),
                          ("kvdec_combine_splits", CombineParams)]:
             f = getattr(lib, name)
@@ -246,6 +248,30 @@ def gqa_decode(q, k, v, seqlens, block_table=None, scale=None, out_dtype=torch.f
     p.workspace = _ptr(workspace)
     p.workspace_bytes = workspace.numel() * workspace.element_size()
     _check(lib.kvdec_gqa_decode(ctypes.byref(p), _stream(stream)), "kvdec_gqa_decode")
+    return out, lse
+
+
+def gqa_decode_noalloc(q, k, v, seqlens, block_table=None, scale=None,
+                       out_dtype=torch.float32, out=None, return_lse=True, error_flag=None,
+                       max_ctas=0, stream=None):
+    """kvdec_gqa_decode_noalloc: the same decode for callers that cannot
+    allocate device memory; the library keeps the split scratch in its own
+    fixed 16 MiB array per GPU, so only inputs and outputs are passed (the
+    tensors returned here are allocated by this Python helper, not by the
+    library).  Calls sharing a device must not overlap on the GPU."""
+    lib = load()
+    dev = q.device
+    for t, n in [(q, "q"), (k, "k"), (v, "v")]:
+        _need(t, n, torch.bfloat16, dev)
+    _need(seqlens, "seqlens", torch.int32, dev)
+    if block_table is not None:
+        _need(block_table, "block_table", torch.int32, dev)
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=dev)
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
+    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas)
+    _check(lib.kvdec_gqa_decode_noalloc(ctypes.byref(p), _stream(stream)),
+           "kvdec_gqa_decode_noalloc")
     return out, lse
 
 

@@ -120,6 +120,35 @@ size_t kvdec_gqa_workspace_bytes(const kvdec_gqa_params* p);
 kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* GQA decode for callers that cannot allocate                               */
+/* ------------------------------------------------------------------------ */
+/*
+ * No counterpart in the source pages: this is a deployment variant of
+ * kvdec_gqa_decode, not part of the method.
+ *
+ * Same operation, arguments and results as kvdec_gqa_decode, for callers that
+ * cannot hand the library a device workspace -- for example a plugin inside
+ * another runtime that owns all device memory through its own allocator, or
+ * a serving loop that commits all free HBM to the KV cache at start-up and
+ * allows no allocation while decoding.  p->workspace and p->workspace_bytes
+ * are ignored: the split scratch lives in a fixed array of
+ * KVDEC_NOALLOC_SCRATCH_BYTES bytes inside the library, held on every GPU
+ * where the library's code is loaded until the process exits.  The call
+ * allocates nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make it before any stream capture there.
+ *   - Problems whose scratch would exceed the array are rejected with
+ *     KVDEC_ERR_WORKSPACE and a message giving the size needed (lower
+ *     max_ctas or batch, or use kvdec_gqa_decode).
+ *   - All calls on a device share the array and it keeps the last call's
+ *     contents; nothing in it needs to start at zero (the split counters
+ *     carry a per-call epoch).  Calls that overlap on the GPU race on it:
+ *     serialise them.
+ */
+#define KVDEC_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+kvdec_status kvdec_gqa_decode_noalloc(const kvdec_gqa_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* MLA absorbed decode                                                       */
 /* ------------------------------------------------------------------------ */
 /*

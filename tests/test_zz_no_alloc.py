@@ -1,0 +1,50 @@
+"""kvdec_gqa_decode_noalloc: the GQA decode for callers that cannot allocate
+device memory (a plugin inside a runtime that owns all device memory, a
+serving loop that allows no allocation while decoding).  It keeps its split
+scratch in a fixed array inside the library, so these tests check, through
+the C ABI, that it gives the same results as kvdec_gqa_decode with a caller
+workspace -- on two calls in a row, the second finding whatever the first
+left in the shared array -- and that problems too big for the array are
+rejected with a clear error.
+
+This file is collected last on purpose: if it fails, a run stopped at the
+first failure has already run every other test."""
+import ctypes
+
+import pytest
+import torch
+
+import kvgen
+from decode_attention_kv_softmax_b300 import kvdec
+from parity import assert_attn_close, assert_lse_close, f64
+
+pytestmark = pytest.mark.gpu
+
+
+def test_matches_workspace_entry_point_on_two_calls(cuda_lib):
+    cases = [
+        # ragged contiguous GQA, sequences cut across CTAs
+        kvgen.gqa_case(4, 32, 8, 128, seqlens=[3000, 1, 700, 4096], cap=4096, seed=71,
+                       device="cuda"),
+        # a different shape next: paged, d = 64, MQA-like group of 16
+        kvgen.gqa_case(3, 16, 1, 64, seqlens=[90, 2000, 5], paged=True, seed=72, device="cuda"),
+    ]
+    for i, case in enumerate(cases):
+        ref, lref = cuda_lib.gqa_decode(case.q, case.k, case.v, case.seqlens, case.block_table,
+                                        scale=case.scale)
+        out, lse = cuda_lib.gqa_decode_noalloc(case.q, case.k, case.v, case.seqlens,
+                                               case.block_table, scale=case.scale)
+        torch.cuda.synchronize()
+        assert_attn_close(out, f64(ref), f"call {i}")
+        assert_lse_close(lse, f64(lref), f"call {i}")
+
+
+def test_rejects_problems_beyond_the_array(cuda_lib):
+    lib = kvdec.load()
+    p = kvdec.GqaParams()
+    # 8192 sequences x 256 KV heads: the split counters alone exceed 16 MiB
+    p.batch, p.num_heads, p.num_kv_heads, p.head_dim, p.capacity = 8192, 256, 256, 128, 64
+    status = lib.kvdec_gqa_decode_noalloc(ctypes.byref(p), None)
+    assert status == 4
+    msg = lib.kvdec_last_error().decode()
+    assert "16777216" in msg and "needs" in msg

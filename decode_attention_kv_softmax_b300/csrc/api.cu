@@ -6,6 +6,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <map>
 #include <mutex>
@@ -146,7 +147,9 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     }
     if (occ < 1) return fail(KVDEC_ERR_CUDA, "GQA kernel does not fit on this device");
     pl.grid = di.sm_count * occ;
-    if (p->max_ctas > 0 && p->max_ctas < pl.grid) pl.grid = p->max_ctas;
+    // max_ctas > 0 sets the number of work items (CTAs); above one resident
+    // wave the hardware hands the equal-size items out as SMs free up.
+    if (p->max_ctas > 0) pl.grid = std::min(p->max_ctas, 64 * di.sm_count * occ);
     const size_t slots = 2 * (size_t)pl.grid;
     pl.off_lse = round_up((size_t)pl.units * 8, 256);
     pl.off_o = pl.off_lse + round_up(slots * pl.hc_rows * 4, 256);
@@ -307,7 +310,12 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
     a.block_table = p->block_table;
     a.num_pages = p->num_pages;
     a.max_blocks = p->max_blocks;
-    a.theta = p->rope_theta != 0.f ? (double)p->rope_theta : 10000.0;
+    const double theta = p->rope_theta != 0.f ? (double)p->rope_theta : 10000.0;
+    const int rot_dim = p->mode == KVDEC_APPEND_MLA ? KVDEC_MLA_DR : p->head_dim;
+    if (rot_dim < 2 || rot_dim > 2 * kvdec::kMaxRopePairs || rot_dim % 2)
+        return fail(KVDEC_ERR_UNSUPPORTED, "rotary dim %d", rot_dim);
+    for (int i = 0; i < rot_dim / 2; ++i)
+        a.inv_freq[i] = std::pow(theta, -2.0 * (double)i / (double)rot_dim);
     a.err = p->error_flag;
     if (p->block_table && (p->num_pages < 1 || p->max_blocks < 1))
         return fail(KVDEC_ERR_INVALID_ARG, "paged append needs num_pages >= 1 and max_blocks >= 1");

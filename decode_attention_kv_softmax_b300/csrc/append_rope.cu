@@ -6,9 +6,10 @@
 //
 // RoPE reading: interleaved pairs (2i, 2i+1) rotated by
 // pos * theta^(-2i/dim).  The angle reaches 1.3e5 rad at 128K context, where
-// a binary32 angle is off by ~1e-2 rad; the angle, its sine/cosine and the
-// rotation are therefore taken in binary64 and rounded once to bf16
-// (nearest-even).  The kernel moves a few KB per call: it is launch-latency
+// a binary32 angle is off by ~1e-2 rad; the angle and its reduction modulo
+// 2 pi are therefore taken in binary64 (the frequencies come from the host
+// in binary64), the sine/cosine of the reduced angle and the rotation in
+// binary32, and the result is rounded once to bf16 (nearest-even).  The kernel moves a few KB per call: it is launch-latency
 // bound, so it is written for simplicity, one CTA per (sequence, head).
 #include "common.cuh"
 #include "kernels.h"
@@ -16,15 +17,18 @@
 namespace kvdec {
 
 
-KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int dim, int pos,
-                            double theta) {
-    const double inv = pow(theta, -2.0 * (double)i / (double)dim);
-    double s, c;
-    sincos((double)pos * inv, &s, &c);
-    const double x0 = (double)__bfloat162float(x[2 * i]);
-    const double x1 = (double)__bfloat162float(x[2 * i + 1]);
-    y[2 * i] = __double2bfloat16(x0 * c - x1 * s);
-    y[2 * i + 1] = __double2bfloat16(x0 * s + x1 * c);
+KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int pos,
+                            const double* inv_freq) {
+    // angle in binary64, reduced to [-pi, pi] in binary64, then sine/cosine
+    // and the rotation in binary32 (|error| ~1e-7, far below one bf16 ulp)
+    const double ang = (double)pos * inv_freq[i];
+    const double r = ang - 6.283185307179586 * rint(ang * 0.15915494309189535);
+    float s, c;
+    sincosf((float)r, &s, &c);
+    const float x0 = __bfloat162float(x[2 * i]);
+    const float x1 = __bfloat162float(x[2 * i + 1]);
+    y[2 * i] = __float2bfloat16_rn(fmaf(x0, c, -x1 * s));
+    y[2 * i + 1] = __float2bfloat16_rn(fmaf(x0, s, x1 * c));
 }
 
 __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
@@ -50,8 +54,7 @@ __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
         const uint4* src = reinterpret_cast<const uint4*>(a.c_kv + (size_t)b * KVDEC_MLA_DC);
         reinterpret_cast<uint4*>(row)[t] = __ldg(src + t);     // 64 threads x 16 B = 512 bf16
         if (t < KVDEC_MLA_DR / 2)
-            rope_pair(a.k_rope + (size_t)b * KVDEC_MLA_DR, row + KVDEC_MLA_DC, t, KVDEC_MLA_DR, pos,
-                      a.theta);
+            rope_pair(a.k_rope + (size_t)b * KVDEC_MLA_DR, row + KVDEC_MLA_DC, t, pos, a.inv_freq);
         return;
     }
     // GQA: K row rotated over the whole head dim, V row copied
@@ -59,7 +62,7 @@ __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
     size_t dst_off;
     if (a.block_table) dst_off = (((size_t)page * a.n_kv + head) * KVDEC_PAGE_SIZE + slot) * a.d;
     else dst_off = (((size_t)b * a.n_kv + head) * a.cap + pos) * a.d;
-    if (t < a.d / 2) rope_pair(a.k_new + src_off, a.k + dst_off, t, a.d, pos, a.theta);
+    if (t < a.d / 2) rope_pair(a.k_new + src_off, a.k + dst_off, t, pos, a.inv_freq);
     if (t < a.d / 8)
         reinterpret_cast<uint4*>(a.v + dst_off)[t] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src_off) + t);
 }

@@ -396,32 +396,46 @@ __global__ void __launch_bounds__(160, 2)
                                            (uint32_t)S.num_pieces(cur.b, cur.j)) ? 1 : 0;
                 named_barrier(1, 128);
                 if (misc[1]) {
-                    // last piece of this unit: merge every piece's partial
+                    // last piece of this unit: merge every piece's partial.
+                    // Piece s lives in slot 2 (w0 + s) (+ kind0 for s = 0).
                     __threadfence();
                     const int np = S.num_pieces(cur.b, cur.j);
-                    for (int i = tid; i < nrows * (D / 4); i += 128) {
-                        const int r = i / (D / 4), c4 = i % (D / 4);
+                    int w0, kind0;
+                    S.first_piece(cur.b, cur.j, w0, kind0);
+                    if (tid < nrows) {
                         float M = -INFINITY;
                         for (int s2 = 0; s2 < np; ++s2) {
-                            const int sl = S.piece_slot(cur.b, cur.j, s2);
-                            M = fmaxf(M, __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r));
+                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
+                            M = fmaxf(M, __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid));
                         }
                         float den = 0.f;
+                        for (int s2 = 0; s2 < np; ++s2) {
+                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
+                            const float ls = __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid);
+                            den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                        }
+                        rowml[tid * 2] = M;
+                        rowml[tid * 2 + 1] = den;
+                        if (a.lse)
+                            a.lse[(size_t)cur.b * a.H + h0 + tid] = (den > 0.f) ? M + __logf(den) : -INFINITY;
+                    }
+                    named_barrier(1, 128);
+                    for (int i = tid; i < nrows * (D / 4); i += 128) {
+                        const int r = i / (D / 4), c4 = i % (D / 4);
+                        const float M = rowml[r * 2], den = rowml[r * 2 + 1];
+                        const float inv = den > 0.f ? 1.f / den : 0.f;
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
                         for (int s2 = 0; s2 < np; ++s2) {
-                            const int sl = S.piece_slot(cur.b, cur.j, s2);
+                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
                             const float ls = __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r);
-                            const float wgt = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                            const float wgt = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * inv;
                             const float4 v = __ldcg(reinterpret_cast<const float4*>(
                                 a.part_o + ((size_t)sl * a.hc_rows + r) * D + c4 * 4));
-                            den += wgt;
                             acc.x = fmaf(wgt, v.x, acc.x);
                             acc.y = fmaf(wgt, v.y, acc.y);
                             acc.z = fmaf(wgt, v.z, acc.z);
                             acc.w = fmaf(wgt, v.w, acc.w);
                         }
-                        const float inv = den > 0.f ? 1.f / den : 0.f;
-                        acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
                         const size_t off = ((size_t)cur.b * a.H + h0 + r) * D + c4 * 4;
                         if (a.out_bf16) {
                             uint2 pk = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
@@ -429,9 +443,6 @@ __global__ void __launch_bounds__(160, 2)
                         } else {
                             *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc;
                         }
-                        if (c4 == 0 && a.lse)
-                            a.lse[(size_t)cur.b * a.H + h0 + r] =
-                                (den > 0.f) ? M + __logf(den) : -INFINITY;
                     }
                     if (tid == 0) a.counters[unit] = 0ull;
                 }

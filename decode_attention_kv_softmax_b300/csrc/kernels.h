@@ -36,13 +36,15 @@ struct CombineArgs {
     int out_bf16;
 };
 
+constexpr int kMaxRopePairs = 64;
+
 struct AppendArgs {
     int mode;  // 0 MLA, 1 GQA
     int B;
     const int32_t* seqlens;
     const int32_t* block_table;
     int num_pages, max_blocks;
-    double theta;
+    double inv_freq[kMaxRopePairs];   // theta^(-2i/dim), computed on the host in binary64
     const __nv_bfloat16* c_kv;
     const __nv_bfloat16* k_rope;
     __nv_bfloat16* cache;

@@ -58,6 +58,13 @@ struct TileSchedule {
         const long long t0 = unit_begin(b, j);
         return item_of(t0 + ntiles(b) - 1) - item_of(t0) + 1;
     }
+    // first item holding unit (b, j) and the slot kind of its first piece;
+    // piece s >= 1 lives in slot 2 * (w0 + s)
+    KVDEC_HDINL void first_piece(int b, int j, int& w0, int& kind0) const {
+        const long long t0 = unit_begin(b, j);
+        w0 = item_of(t0);
+        kind0 = (t0 != item_begin(w0)) ? 1 : 0;
+    }
     KVDEC_HDINL int piece_slot(int b, int j, int s) const {
         const long long t0 = unit_begin(b, j);
         const int w0 = item_of(t0);
@@ -99,7 +106,9 @@ KVDEC_DEVINL int clamp_len(int len, int cap, uint32_t* err) {
 }
 
 // Block-wide: cum[0..B] from seqlens (clamped to cap).  `scratch` holds
-// blockDim.x ints.  Ends with __syncthreads().
+// blockDim.x ints (blockDim.x <= 256).  Each thread sums a contiguous chunk of
+// sequences, warp 0 scans the per-thread sums with shuffles, and each thread
+// writes its chunk's prefix.  Ends with __syncthreads().
 KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int B, int cap,
                             uint32_t* err) {
     const int tid = threadIdx.x, nth = blockDim.x;
@@ -112,14 +121,33 @@ KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int 
     }
     scratch[tid] = sum;
     __syncthreads();
-    if (tid == 0) {
-        int run = 0;
-        for (int i = 0; i < nth; ++i) {
-            const int v = scratch[i];
-            scratch[i] = run;
-            run += v;
+    if (tid < 32) {
+        // lane l owns scratch[l*per .. l*per + per)
+        const int per = (nth + 31) / 32;
+        int v[8];
+        int tot = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int idx = tid * per + k;
+            v[k] = (k < per && idx < nth) ? scratch[idx] : 0;
+            tot += v[k];
         }
-        cum[B] = run;
+        int incl = tot;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, incl, off);
+            if (tid >= off) incl += u;
+        }
+        int run = incl - tot;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int idx = tid * per + k;
+            if (k < per && idx < nth) {
+                scratch[idx] = run;
+                run += v[k];
+            }
+        }
+        if (tid == 31) cum[B] = incl;
     }
     __syncthreads();
     int run = scratch[tid];

@@ -112,7 +112,7 @@ typedef struct kvdec_gqa_params {
     void* workspace;
     size_t workspace_bytes;
     uint32_t* error_flag;    /* optional */
-    int32_t max_ctas;        /* 0 = one full wave of resident CTAs */
+    int32_t max_ctas;        /* work items (CTAs); 0 = one wave of resident CTAs */
     int32_t reserved;
 } kvdec_gqa_params;
 

@@ -99,6 +99,11 @@ static void run_case(const std::vector<int>& lens, int upb, int grid, int min_ti
             }
             std::set<int> want;
             for (int s = 0; s < np; ++s) want.insert(S.piece_slot(b, j, s));
+            int w0, kind0;
+            S.first_piece(b, j, w0, kind0);
+            for (int s = 0; s < np; ++s)
+                CHECK(S.piece_slot(b, j, s) == 2 * (w0 + s) + (s == 0 ? kind0 : 0),
+                      "unit (%d,%d) first_piece progression", b, j);
             CHECK(want == slots_of_unit[key], "unit (%d,%d) slots", b, j);
             CHECK((int)want.size() == np, "unit (%d,%d) piece count", b, j);
         }

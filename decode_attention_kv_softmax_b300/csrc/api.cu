@@ -310,12 +310,6 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
     a.block_table = p->block_table;
     a.num_pages = p->num_pages;
     a.max_blocks = p->max_blocks;
-    const double theta = p->rope_theta != 0.f ? (double)p->rope_theta : 10000.0;
-    const int rot_dim = p->mode == KVDEC_APPEND_MLA ? KVDEC_MLA_DR : p->head_dim;
-    if (rot_dim < 2 || rot_dim > 2 * kvdec::kMaxRopePairs || rot_dim % 2)
-        return fail(KVDEC_ERR_UNSUPPORTED, "rotary dim %d", rot_dim);
-    for (int i = 0; i < rot_dim / 2; ++i)
-        a.inv_freq[i] = std::pow(theta, -2.0 * (double)i / (double)rot_dim);
     a.err = p->error_flag;
     if (p->block_table && (p->num_pages < 1 || p->max_blocks < 1))
         return fail(KVDEC_ERR_INVALID_ARG, "paged append needs num_pages >= 1 and max_blocks >= 1");
@@ -350,6 +344,12 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
     } else {
         return fail(KVDEC_ERR_INVALID_ARG, "mode %d", p->mode);
     }
+    const double theta = p->rope_theta != 0.f ? (double)p->rope_theta : 10000.0;
+    const int rot_dim = p->mode == KVDEC_APPEND_MLA ? KVDEC_MLA_DR : p->head_dim;
+    if (rot_dim < 2 || rot_dim > 2 * kvdec::kMaxRopePairs || rot_dim % 2)
+        return fail(KVDEC_ERR_UNSUPPORTED, "rotary dim %d", rot_dim);
+    for (int i = 0; i < rot_dim / 2; ++i)
+        a.inv_freq[i] = std::pow(theta, -2.0 * (double)i / (double)rot_dim);
     cudaError_t e = kvdec::launch_append(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     return KVDEC_OK;

@@ -157,6 +157,48 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     return KVDEC_OK;
 }
 
+// ---------------------------------------------------------------- MLA layout
+
+struct MlaPlan {
+    int pairs;
+    size_t off_lse, off_o, bytes;
+};
+
+constexpr int kMaxBatchMla = 2048;
+
+kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "params is NULL");
+    if (p->num_heads != 128)
+        return fail(KVDEC_ERR_UNSUPPORTED, "num_heads %d (the MLA kernel is built for 128)", p->num_heads);
+    if (p->batch < 1 || p->batch > kMaxBatchMla)
+        return fail(KVDEC_ERR_INVALID_ARG, "batch %d outside [1, %d]", p->batch, kMaxBatchMla);
+    if (p->num_pages < 1 || p->max_blocks < 1)
+        return fail(KVDEC_ERR_INVALID_ARG, "num_pages and max_blocks must be >= 1");
+    DeviceInfo di;
+    int dev;
+    if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
+    int pairs;
+    {
+        auto key = std::make_tuple(dev, 1, 0, 0, p->batch);
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it == g_occupancy.end()) {
+            pairs = kvdec::max_pairs_mla(p->batch);
+            g_occupancy[key] = pairs;
+        } else {
+            pairs = it->second;
+        }
+    }
+    if (pairs < 1) return fail(KVDEC_ERR_CUDA, "MLA kernel clusters do not fit on this device");
+    if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
+    pl.pairs = pairs;
+    const size_t slots = 2 * (size_t)pairs;
+    pl.off_lse = round_up((size_t)p->batch * 2 * 4 * 8, 256);
+    pl.off_o = pl.off_lse + round_up(2 * slots * 128 * 4, 256);
+    pl.bytes = pl.off_o + slots * 128 * 512 * 4;
+    return KVDEC_OK;
+}
+
 }  // namespace
 
 namespace kvdec {
@@ -269,6 +311,67 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
     a.timeout_ns = kvdec::kDefaultTimeoutNs;
     cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, tk, tv, a, pl.grid, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
+    return KVDEC_OK;
+}
+
+
+size_t kvdec_mla_workspace_bytes(const kvdec_mla_params* p) {
+    MlaPlan pl;
+    if (plan_mla(p, pl) != KVDEC_OK) return 0;
+    return pl.bytes;
+}
+
+kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) {
+    MlaPlan pl;
+    kvdec_status st = plan_mla(p, pl);
+    if (st != KVDEC_OK) return st;
+    if (!p->q_absorbed || !p->q_rope || !p->cache || !p->block_table || !p->seqlens || !p->out)
+        return fail(KVDEC_ERR_INVALID_ARG,
+                    "q_absorbed, q_rope, cache, block_table, seqlens and out must be non-NULL");
+    if (!aligned(p->q_absorbed, 16) || !aligned(p->q_rope, 16) || !aligned(p->cache, 16) ||
+        !aligned(p->out, 16))
+        return fail(KVDEC_ERR_INVALID_ARG, "q_absorbed, q_rope, cache and out must be 16-byte aligned");
+    if (!aligned(p->block_table, 4) || !aligned(p->seqlens, 4) || (p->lse && !aligned(p->lse, 4)))
+        return fail(KVDEC_ERR_INVALID_ARG, "block_table, seqlens and lse must be 4-byte aligned");
+    if (p->out_dtype != KVDEC_F32 && p->out_dtype != KVDEC_BF16)
+        return fail(KVDEC_ERR_INVALID_ARG, "out_dtype %d", p->out_dtype);
+    if (!p->workspace || !aligned(p->workspace, 256))
+        return fail(KVDEC_ERR_WORKSPACE, "workspace must be non-NULL and 256-byte aligned");
+    if (p->workspace_bytes < pl.bytes)
+        return fail(KVDEC_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", p->workspace_bytes,
+                    pl.bytes);
+    const uint64_t rows = (uint64_t)p->num_pages * KVDEC_PAGE_SIZE;
+    if (rows >= 0x7fffffffull || (uint64_t)p->max_blocks * KVDEC_PAGE_SIZE >= 0x7fffffffull)
+        return fail(KVDEC_ERR_UNSUPPORTED, "cache too large (rows >= 2^31)");
+    kvdec::MlaMaps maps;
+    const uint64_t qrows = (uint64_t)p->batch * 128;
+    if ((st = encode_2d(&maps.qa, p->q_absorbed, qrows, 512, 1024, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
+        return st;
+    if ((st = encode_2d(&maps.qr, p->q_rope, qrows, 64, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+    if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+    if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+    kvdec::MlaArgs a;
+    memset(&a, 0, sizeof(a));
+    a.block_table = p->block_table;
+    a.seqlens = p->seqlens;
+    a.out = p->out;
+    a.lse = p->lse;
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    a.counters = reinterpret_cast<unsigned long long*>(ws);
+    a.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
+    a.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+    a.epoch = next_epoch();
+    a.err = p->error_flag;
+    a.B = p->batch;
+    a.num_pages = p->num_pages;
+    a.max_blocks = p->max_blocks;
+    a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
+    a.scale_log2 = (float)(scale * 1.4426950408889634);
+    a.min_tiles = 4;
+    a.timeout_ns = kvdec::kDefaultTimeoutNs;
+    cudaError_t e = kvdec::launch_mla(maps, a, pl.pairs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
     return KVDEC_OK;
 }
 

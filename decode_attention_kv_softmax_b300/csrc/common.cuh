@@ -89,6 +89,69 @@ KVDEC_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abo
     return false;
 }
 
+// ---------------------------------------------------------------- clusters
+
+KVDEC_DEVINL uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+KVDEC_DEVINL uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+KVDEC_DEVINL void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
+                 "f"(d)
+                 : "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+KVDEC_DEVINL void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+KVDEC_DEVINL bool mbar_try_wait_acq_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on a local barrier whose phases are completed by arrivals
+// from another CTA of the cluster (acquire at cluster scope).
+KVDEC_DEVINL bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_word,
+                                        uint32_t* err, uint64_t timeout_ns) {
+    if (*abort_word) return false;
+    if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_acq_cluster(bar, parity)) return true;
+        if (*abort_word) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_word = 1;
+            report(err, KVDEC_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+KVDEC_DEVINL void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 
 KVDEC_DEVINL uint64_t l2_policy_evict_first() {

@@ -56,6 +56,33 @@ struct AppendArgs {
     uint32_t* err;
 };
 
+struct MlaMaps {
+    CUtensorMap qa;    // q_absorbed [B*128, 512], box 64 x 128, 128-byte swizzle
+    CUtensorMap qr;    // q_rope [B*128, 64], box 32 x 128, 64-byte swizzle
+    CUtensorMap c128;  // cache [pages*64, 576], box 64 x 64, 128-byte swizzle
+    CUtensorMap c64;   // cache [pages*64, 576], box 32 x 64, 64-byte swizzle
+};
+
+struct MlaArgs {
+    const int32_t* block_table;
+    const int32_t* seqlens;
+    void* out;
+    float* lse;
+    float* part_o;                  // [2*pairs, 128, 512]
+    float* part_lse;                // [2 halves][2*pairs, 128]
+    unsigned long long* counters;   // [B][2 halves][4 head quarters]
+    uint32_t epoch;
+    uint32_t* err;
+    int B, num_pages, max_blocks;
+    int out_bf16;
+    float scale_log2;
+    int min_tiles;
+    uint64_t timeout_ns;
+};
+
+cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st);
+int max_pairs_mla(int B);
+
 cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st);
 int occupancy_gqa(int D, int MT, int B);

@@ -1,0 +1,114 @@
+"""GPU parity of kvdec_mla_decode_absorbed (tcgen05 MLA decode over the paged
+576-wide latent cache) against the fp64 oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import kvgen
+import oracle
+from parity import (assert_attn_close, assert_lse_close, f64, mla_rows_oracle,
+                    sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+def run(kv, case, **kw):
+    out, lse = kv.mla_decode_absorbed(case.q_abs, case.q_rope, case.cache, case.block_table,
+                                      case.seqlens, scale=case.scale, **kw)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def full_oracle(case):
+    return oracle.mla_decode_absorbed(f64(case.q_abs), f64(case.q_rope), f64(case.cache),
+                                      case.block_table.cpu().numpy(), case.seqlens.cpu().numpy(),
+                                      case.scale)
+
+
+@pytest.mark.parametrize("sl", [[100, 700], [1, 64, 65], [64], [3000, 17, 129, 4096]])
+def test_small_full_parity(cuda_lib, sl):
+    case = kvgen.mla_case(len(sl), 128, seqlens=sl, seed=200 + len(sl), device="cuda")
+    out, lse = run(cuda_lib, case)
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref, "mla")
+    assert_lse_close(lse, lref, "mla lse")
+
+
+@pytest.mark.parametrize("max_ctas", [2, 4, 6, 14, 0])
+def test_split_invariance(cuda_lib, max_ctas):
+    """Sequences cut across CTA pairs merge to the same result."""
+    case = kvgen.mla_case(3, 128, seqlens=[2500, 640, 5], seed=211, device="cuda")
+    ref, lref = full_oracle(case)
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas)
+    assert_attn_close(out, ref, f"max_ctas={max_ctas}")
+    assert_lse_close(lse, lref)
+
+
+def test_empty_sequences_and_bf16(cuda_lib):
+    case = kvgen.mla_case(3, 128, seqlens=[0, 300, 0], seed=212, device="cuda")
+    out, lse = run(cuda_lib, case, out_dtype=torch.bfloat16)
+    assert out.dtype == torch.bfloat16
+    assert torch.all(out[0] == 0) and torch.all(out[2] == 0)
+    assert torch.isneginf(lse[0]).all() and torch.isneginf(lse[2]).all()
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref, "bf16")
+    assert_lse_close(lse, lref)
+
+
+def test_default_scale_is_192(cuda_lib):
+    """scale 0 selects 1/sqrt(128 + 64) ([ARG] §四.5)."""
+    case = kvgen.mla_case(1, 128, seqlens=[333], seed=213, device="cuda")
+    out, _ = cuda_lib.mla_decode_absorbed(case.q_abs, case.q_rope, case.cache, case.block_table,
+                                          case.seqlens)
+    torch.cuda.synchronize()
+    ref, _ = full_oracle(case)
+    assert_attn_close(out, ref)
+
+
+def test_shared_pages(cuda_lib):
+    case = kvgen.mla_case(2, 128, seqlens=[700, 700], seed=214, device="cuda")
+    case.block_table[1] = case.block_table[0]
+    case.q_abs[1] = case.q_abs[0]
+    case.q_rope[1] = case.q_rope[0]
+    out, _ = run(cuda_lib, case)
+    assert_attn_close(out[0], f64(out[1]), "aliased pages", atol=5e-3, row_rtol=5e-3)
+    ref, _ = full_oracle(case)
+    assert_attn_close(out, ref)
+
+
+def test_rope_part_is_used(cuda_lib):
+    """Zeroing q_rope changes the result exactly as the oracle says: the
+    decoupled rope term of the score is not dropped."""
+    case = kvgen.mla_case(2, 128, seqlens=[400, 90], seed=215, device="cuda")
+    case.q_rope.mul_(8.0)
+    out, _ = run(cuda_lib, case)
+    ref, _ = full_oracle(case)
+    assert_attn_close(out, ref, "scaled rope")
+    case.q_rope.zero_()
+    out0, _ = run(cuda_lib, case)
+    ref0, _ = full_oracle(case)
+    assert_attn_close(out0, ref0, "no rope")
+    assert np.abs(ref - ref0).max() > 0.05
+
+
+@pytest.mark.parametrize("name", ["C3", "C4-MLA"])
+def test_full_size_sampled(cuda_lib, name):
+    case = kvgen.config_case(name, device="cuda")
+    out, lse = run(cuda_lib, case)
+    rows = sample_rows(case.B, case.n_h, 24, seed=7 + len(name))
+    ref, lref = mla_rows_oracle(case, rows)
+    got = torch.stack([out[b, h] for b, h in rows])
+    assert_attn_close(got, ref, name)
+    assert_lse_close(torch.stack([lse[b, h] for b, h in rows]), lref, name)
+    assert torch.isfinite(out).all()
+
+
+def test_bad_page_reported(cuda_lib):
+    case = kvgen.mla_case(2, 128, seqlens=[200, 100], seed=216, device="cuda")
+    case.block_table[0, 1] = case.cache.shape[0] + 3
+    flag = cuda_lib.new_error_flag()
+    out, _ = cuda_lib.mla_decode_absorbed(case.q_abs, case.q_rope, case.cache, case.block_table,
+                                          case.seqlens, error_flag=flag)
+    torch.cuda.synchronize()
+    assert flag.item() & cuda_lib.DEVERR_BAD_PAGE
+    assert torch.isfinite(out).all()

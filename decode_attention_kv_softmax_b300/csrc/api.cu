@@ -193,8 +193,8 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
     if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
     pl.pairs = pairs;
     const size_t slots = 2 * (size_t)pairs;
-    pl.off_lse = round_up((size_t)p->batch * 2 * 4 * 8, 256);
-    pl.off_o = pl.off_lse + round_up(2 * slots * 128 * 4, 256);
+    pl.off_lse = round_up((size_t)p->batch * 2 * 8 * 8, 256);
+    pl.off_o = pl.off_lse + round_up(4 * slots * 128 * 4, 256);
     pl.bytes = pl.off_o + slots * 128 * 512 * 4;
     return KVDEC_OK;
 }
@@ -344,14 +344,12 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     if (rows >= 0x7fffffffull || (uint64_t)p->max_blocks * KVDEC_PAGE_SIZE >= 0x7fffffffull)
         return fail(KVDEC_ERR_UNSUPPORTED, "cache too large (rows >= 2^31)");
     kvdec::MlaMaps maps;
-    const uint64_t qrows = (uint64_t)p->batch * 128;
-    if ((st = encode_2d(&maps.qa, p->q_absorbed, qrows, 512, 1024, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)))
-        return st;
-    if ((st = encode_2d(&maps.qr, p->q_rope, qrows, 64, 128, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
     if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
     kvdec::MlaArgs a;
     memset(&a, 0, sizeof(a));
+    a.q_abs = static_cast<const __nv_bfloat16*>(p->q_absorbed);
+    a.q_rope = static_cast<const __nv_bfloat16*>(p->q_rope);
     a.block_table = p->block_table;
     a.seqlens = p->seqlens;
     a.out = p->out;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -108,6 +109,22 @@ KVDEC_DEVINL void st_cluster_f4(uint32_t addr, float a, float b, float c, float 
     asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c),
                  "f"(d)
                  : "memory");
+}
+
+// Asynchronous store of 16 bytes into another CTA's shared memory; the
+// bytes are counted as transaction bytes on that CTA's mbarrier `rbar`.
+KVDEC_DEVINL void st_async_f4(uint32_t addr, float a, float b, float c, float d, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
+        : "memory");
+}
+
+KVDEC_DEVINL void st_async_u4(uint32_t addr, uint4 v, uint32_t rbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+        "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+        : "memory");
 }
 
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
@@ -220,6 +237,15 @@ KVDEC_DEVINL float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+KVDEC_DEVINL uint32_t pack_half2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+KVDEC_DEVINL float2 unpack_half2(uint32_t u) {
+    return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 
 KVDEC_DEVINL uint32_t pack_bf16x2(float lo, float hi) {

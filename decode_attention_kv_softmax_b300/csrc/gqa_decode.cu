@@ -102,7 +102,9 @@ __global__ void __launch_bounds__(160, 2)
             const int kvh = cur.j / a.n_hc;
             int row;
             if (a.paged) {
-                int page = __ldg(a.block_table + (size_t)cur.b * a.max_blocks + cur.lt);
+                int page = (cur.b < a.B && cur.lt < a.max_blocks)
+                               ? __ldg(a.block_table + (size_t)cur.b * a.max_blocks + cur.lt)
+                               : -1;
                 if (page < 0 || page >= a.num_pages) {
                     report(a.err, KVDEC_DEVERR_BAD_PAGE);
                     page = 0;

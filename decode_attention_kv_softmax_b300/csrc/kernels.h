@@ -57,20 +57,20 @@ struct AppendArgs {
 };
 
 struct MlaMaps {
-    CUtensorMap qa;    // q_absorbed [B*128, 512], box 64 x 128, 128-byte swizzle
-    CUtensorMap qr;    // q_rope [B*128, 64], box 32 x 128, 64-byte swizzle
     CUtensorMap c128;  // cache [pages*64, 576], box 64 x 64, 128-byte swizzle
     CUtensorMap c64;   // cache [pages*64, 576], box 32 x 64, 64-byte swizzle
 };
 
 struct MlaArgs {
+    const __nv_bfloat16* q_abs;     // [B, 128, 512]
+    const __nv_bfloat16* q_rope;    // [B, 128, 64]
     const int32_t* block_table;
     const int32_t* seqlens;
     void* out;
     float* lse;
     float* part_o;                  // [2*pairs, 128, 512]
-    float* part_lse;                // [2 halves][2*pairs, 128]
-    unsigned long long* counters;   // [B][2 halves][4 head quarters]
+    float* part_lse;                // [2 CTAs][2 column halves][2*pairs, 128]
+    unsigned long long* counters;   // [B][2 CTAs][8 softmax warps]
     uint32_t epoch;
     uint32_t* err;
     int B, num_pages, max_blocks;

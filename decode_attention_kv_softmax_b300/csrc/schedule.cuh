@@ -106,7 +106,7 @@ KVDEC_DEVINL int clamp_len(int len, int cap, uint32_t* err) {
 }
 
 // Block-wide: cum[0..B] from seqlens (clamped to cap).  `scratch` holds
-// blockDim.x ints (blockDim.x <= 256).  Each thread sums a contiguous chunk of
+// blockDim.x ints.  Each thread sums a contiguous chunk of
 // sequences, warp 0 scans the per-thread sums with shuffles, and each thread
 // writes its chunk's prefix.  Ends with __syncthreads().
 KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int B, int cap,
@@ -122,16 +122,11 @@ KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int 
     scratch[tid] = sum;
     __syncthreads();
     if (tid < 32) {
-        // lane l owns scratch[l*per .. l*per + per)
+        // lane l owns scratch[l*per .. l*per + per), any block size
         const int per = (nth + 31) / 32;
-        int v[8];
+        const int lo_i = min(nth, tid * per), hi_i = min(nth, lo_i + per);
         int tot = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int idx = tid * per + k;
-            v[k] = (k < per && idx < nth) ? scratch[idx] : 0;
-            tot += v[k];
-        }
+        for (int idx = lo_i; idx < hi_i; ++idx) tot += scratch[idx];
         int incl = tot;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -139,13 +134,10 @@ KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int 
             if (tid >= off) incl += u;
         }
         int run = incl - tot;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int idx = tid * per + k;
-            if (k < per && idx < nth) {
-                scratch[idx] = run;
-                run += v[k];
-            }
+        for (int idx = lo_i; idx < hi_i; ++idx) {
+            const int v = scratch[idx];
+            scratch[idx] = run;
+            run += v;
         }
         if (tid == 31) cum[B] = incl;
     }

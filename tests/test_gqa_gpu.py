@@ -50,6 +50,19 @@ def test_small_full_parity(cuda_lib, B, h, n_kv, d, sl, paged):
     assert_lse_close(lse, lref, "lse")
 
 
+def test_many_short_sequences(cuda_lib):
+    """Hundreds of sequences: every thread of the block-wide tile scan
+    carries a sequence."""
+    g = torch.Generator().manual_seed(6)
+    sl = torch.randint(0, 300, (900,), generator=g).tolist()
+    case = kvgen.gqa_case(len(sl), 8, 2, 64, seqlens=sl, paged=True, seed=121, device="cuda")
+    out, lse = run(cuda_lib, case)
+    rows = sample_rows(case.B, case.h, 64, seed=4)
+    ref, lref = gqa_rows_oracle(case, rows)
+    assert_attn_close(torch.stack([out[b, h] for b, h in rows]), ref, "many")
+    assert_lse_close(torch.stack([lse[b, h] for b, h in rows]), lref)
+
+
 def test_tiny_config(cuda_lib):
     case = kvgen.config_case("C0", device="cuda")
     out, lse = run(cuda_lib, case)

@@ -34,6 +34,21 @@ def test_small_full_parity(cuda_lib, sl):
     assert_lse_close(lse, lref, "mla lse")
 
 
+def test_many_short_sequences(cuda_lib):
+    """Hundreds of sequences: every thread of the block-wide tile scan
+    carries a sequence."""
+    g = torch.Generator().manual_seed(5)
+    sl = torch.randint(0, 200, (700,), generator=g).tolist()
+    case = kvgen.mla_case(len(sl), 128, seqlens=sl, seed=217, device="cuda")
+    out, lse = run(cuda_lib, case)
+    rows = sample_rows(case.B, case.n_h, 64, seed=3)
+    ref, lref = mla_rows_oracle(case, rows)
+    assert_attn_close(torch.stack([out[b, h] for b, h in rows]), ref, "many")
+    assert_lse_close(torch.stack([lse[b, h] for b, h in rows]), lref)
+    empty = [b for b, s in enumerate(sl) if s == 0]
+    assert all(torch.all(out[b] == 0) for b in empty[:5])
+
+
 @pytest.mark.parametrize("max_ctas", [2, 4, 6, 14, 0])
 def test_split_invariance(cuda_lib, max_ctas):
     """Sequences cut across CTA pairs merge to the same result."""

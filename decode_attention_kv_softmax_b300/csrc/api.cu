@@ -157,6 +157,9 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     return KVDEC_OK;
 }
 
+// The kernels take the row max before scaling, so the scale must be positive.
+bool scale_ok(float s) { return s == 0.f || (s > 0.f && std::isfinite(s)); }
+
 // ---------------------------------------------------------------- MLA layout
 
 struct MlaPlan {
@@ -193,8 +196,8 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
     if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
     pl.pairs = pairs;
     const size_t slots = 2 * (size_t)pairs;
-    pl.off_lse = round_up((size_t)p->batch * 2 * 8 * 8, 256);
-    pl.off_o = pl.off_lse + round_up(4 * slots * 128 * 4, 256);
+    pl.off_lse = round_up((size_t)p->batch * 2 * 4 * 8, 256);
+    pl.off_o = pl.off_lse + round_up(2 * slots * 128 * 4, 256);
     pl.bytes = pl.off_o + slots * 128 * 512 * 4;
     return KVDEC_OK;
 }
@@ -305,6 +308,7 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
     a.num_pages = p->num_pages;
     a.max_blocks = p->max_blocks;
     a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    if (!scale_ok(p->scale)) return fail(KVDEC_ERR_INVALID_ARG, "scale %g (must be 0 or positive and finite)", (double)p->scale);
     const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt((double)pl.D);
     a.scale_log2 = (float)(scale * 1.4426950408889634);
     a.min_tiles = 8;
@@ -364,6 +368,7 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     a.num_pages = p->num_pages;
     a.max_blocks = p->max_blocks;
     a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    if (!scale_ok(p->scale)) return fail(KVDEC_ERR_INVALID_ARG, "scale %g (must be 0 or positive and finite)", (double)p->scale);
     const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
     a.scale_log2 = (float)(scale * 1.4426950408889634);
     a.min_tiles = 4;

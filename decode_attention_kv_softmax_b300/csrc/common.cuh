@@ -64,6 +64,20 @@ KVDEC_DEVINL bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity (never suspends the
+// thread, unlike try_wait): for polling loops that have other work to do.
+KVDEC_DEVINL bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // timeout_ns and returns false (the caller reports and unwinds).
 KVDEC_DEVINL bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t timeout_ns) {
@@ -84,10 +98,19 @@ KVDEC_DEVINL bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t time
 KVDEC_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_word,
                                 uint32_t* err, uint64_t timeout_ns) {
     if (*abort_word) return false;
-    if (mbar_wait_bounded(bar, parity, timeout_ns)) return true;
-    *abort_word = 1;
-    report(err, KVDEC_DEVERR_TIMEOUT);
-    return false;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_word) return false;
+        if (global_timer_ns() - t0 > timeout_ns) {
+            *abort_word = 1;
+            report(err, KVDEC_DEVERR_TIMEOUT);
+            return false;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- clusters
@@ -125,6 +148,15 @@ KVDEC_DEVINL void st_async_u4(uint32_t addr, uint4 v, uint32_t rbar) {
         "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
         "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
         : "memory");
+}
+
+// Relaxed arrive on an mbarrier of another CTA of the cluster: orders
+// nothing, so it does not wait for this thread's outstanding remote stores.
+// Used only to hand back a buffer whose loads have already returned their
+// values (a warp issues in order, and those values have been consumed).
+KVDEC_DEVINL void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
 }
 
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.

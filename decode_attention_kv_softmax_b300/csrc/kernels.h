@@ -69,8 +69,8 @@ struct MlaArgs {
     void* out;
     float* lse;
     float* part_o;                  // [2*pairs, 128, 512]
-    float* part_lse;                // [2 CTAs][2 column halves][2*pairs, 128]
-    unsigned long long* counters;   // [B][2 CTAs][8 softmax warps]
+    float* part_lse;                // [2 CTAs][2*pairs, 128]
+    unsigned long long* counters;   // [B][2 CTAs][4 head quadrants]
     uint32_t epoch;
     uint32_t* err;
     int B, num_pages, max_blocks;

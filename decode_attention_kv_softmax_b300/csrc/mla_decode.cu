@@ -19,20 +19,23 @@
 // run the same online softmax on S = S_0 + S_1, and each accumulates
 // O_r += P V_r for its own 256 output columns (M=128, N=256, K=64).  Every
 // cache byte is read from HBM once and no MMA is duplicated.
-//   TMEM per CTA (512 columns): O_r [0,256), Q_r [256,400) (bf16 pairs),
-//   S [400,464), P [464,496) (bf16 pairs).  Both MMAs take their A operand
-//   (Q, P) from TMEM, so shared memory holds only cache pages (five 36 KB
-//   stages, TMA with 128/64-byte swizzle) and two 16 KB exchange buffers.
-// The partial-S exchange is pipelined one page ahead: while a page's
-// softmax runs, the next page's partial S already travels to the peer (as
-// fp16) with asynchronous remote stores that complete on the peer's
-// mbarrier; the MMA thread keeps S up to two pages ahead of PV.
-// Roles: warps 0-7 run the softmax, two warps per TMEM lane quadrant (one
-// head per lane, 32 of the 64 columns each; the row max is shared through a
-// small buffer); warp 8 issues the MMAs (one thread) and owns the TMEM
-// allocation; warp 9 issues the TMA loads (one thread).  Softmax is base 2
-// with lazy rescaling: O is rescaled only when a row's running max grows by
-// more than 2^8.
+//   TMEM per CTA (512 columns): O_r [0,256), the 256 latent dims of Q_r
+//   [256,384) (bf16 pairs), and two S buffers [384,448), [448,512), one per
+//   softmax group; P (bf16 pairs) overwrites the first 32 columns of its S.
+//   The 32 rope dims of Q_r sit in shared memory (8 KB), beside five (four
+//   for very large batches) 36 KB cache stages (TMA, 128/64-byte swizzle)
+//   and two 16 KB exchange buffers.
+// The partial S travels to the peer as fp16 with asynchronous remote stores
+// that complete on the peer's mbarrier; with two groups, one page's exchange
+// overlaps the other page's softmax.  The MMA thread keeps S up to two pages
+// ahead of PV.
+// Roles: warps 0-7 run the softmax in two groups of four that take
+// alternate pages (ping-pong); in a group, thread i owns head i (TMEM lane i)
+// and all 64 columns of the page.  Only the running max and the running sum
+// pass from one group to the other, through a small hand-off buffer.  Warp 8
+// issues the MMAs (one thread) and owns the TMEM allocation; warp 9 issues
+// the TMA loads (one thread).  Softmax is base 2 with lazy rescaling: O is
+// rescaled only when a row's running max grows by more than 2^8.
 // The split-KV schedule (schedule.cuh) gives each CTA pair an equal share of
 // all pages; sequences cut across pairs leave normalised partials, merged by
 // log-sum-exp ([ARG] §五.2) by the last piece to finish, per warp tile.
@@ -45,76 +48,81 @@ namespace kvdec {
 
 namespace mla {
 constexpr int kHeads = 128;
-constexpr int kNS = 5;                          // cache stages
 constexpr int kStageBytes = 4 * 8192 + 4096;    // c_kv 4 x [64 x 64] SW128 + rope [64 x 32] SW64
-constexpr int kOffKV = 0;
-constexpr int kOffRecv = kOffKV + kNS * kStageBytes;          // [2][8][128] uint4 (8 fp16) partial S
-constexpr int kRecvBytes = 8 * kHeads * 16;                   // one buffer
-constexpr int kOffRed = kOffRecv + 2 * kRecvBytes;            // row max: [2 parity][2 halves][128]
-constexpr int kOffRedL = kOffRed + 2 * 2 * kHeads * 4;        // row sum at a flush: [2 halves][128]
-constexpr int kOffBars = kOffRedL + 2 * kHeads * 4;
-enum {
-    B_Q_FULL, B_Q_FREE, B_KV_FULL, B_KV_EMPTY = B_KV_FULL + kNS, B_S_FULL = B_KV_EMPTY + kNS,
-    B_S_FREE, B_P_FULL, B_P_FREE, B_O_FREE, B_RECV_FULL, B_RECV_EMPTY = B_RECV_FULL + 2,
-    B_PAIR = B_RECV_EMPTY + 2, B_DONE = B_PAIR + 4,
-    B_COUNT
-};
-constexpr int kOffMisc = kOffBars + B_COUNT * 8;   // [0] TMEM base, [1] abort word
-constexpr int kSoftWarps = 8;
+constexpr int kRecvBytes = 8 * kHeads * 16;     // one exchange buffer: [8][128] uint4 (8 fp16)
+constexpr int kQRBytes = kHeads * 64;           // q_rope [128 x 32] bf16, K-major SW64
+constexpr int kHandBytes = 2 * 2 * kHeads * 8;  // hand-off: [2 groups][2][128] (m, l)
+constexpr int kSoftWarps = 8;                   // two groups of four
+constexpr int kGroupWarps = 4;
 constexpr int kThreads = 32 * (kSoftWarps + 2);
-constexpr int kOffScratch = kOffMisc + 16;
-constexpr int kOffCum = kOffScratch + kThreads * 4;
-constexpr int smem_bytes(int B) { return kOffCum + (B + 1) * 4 + 1024; }
+enum {
+    B_Q_FULL, B_S_FULL, B_P_FULL = B_S_FULL + 2, B_PV_DONE = B_P_FULL + 2, B_O_FREE = B_PV_DONE + 2,
+    B_RECV_FULL, B_RECV_EMPTY = B_RECV_FULL + 2, B_HAND = B_RECV_EMPTY + 2,   // [4 quadrants][2 groups][2]
+    B_DONE = B_HAND + 16, B_KV = B_DONE + 1                                    // then full[NS], empty[NS]
+};
+template <int NS>
+struct Layout {
+    static constexpr int kOffKV = 0;
+    static constexpr int kOffRecv = NS * kStageBytes;
+    static constexpr int kOffQR = kOffRecv + 2 * kRecvBytes;
+    static constexpr int kOffHand = kOffQR + kQRBytes;
+    static constexpr int kOffBars = kOffHand + kHandBytes;
+    static constexpr int kBars = B_KV + 2 * NS;
+    static constexpr int kOffMisc = kOffBars + ((kBars * 8 + 15) & ~15);   // [0] TMEM base, [1] abort word
+    static constexpr int kOffCum = kOffMisc + 16;
+    static constexpr int smem_bytes(int B) { return kOffCum + (B + 1) * 4 + 1024; }
+    static_assert(kOffRecv % 1024 == 0 && kOffQR % 1024 == 0, "alignment");
+    static_assert(kThreads * 4 <= 2 * kRecvBytes, "scan scratch lives in the exchange buffers");
+};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemQ = 256;
-constexpr uint32_t kTmemS = 400;
-constexpr uint32_t kTmemP = 464;
-static_assert(kStageBytes % 1024 == 0 && kOffRecv % 1024 == 0, "alignment");
-static_assert(kOffBars % 8 == 0, "alignment");
+constexpr uint32_t kTmemS = 384;
 }  // namespace mla
 
+template <int NS>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ MlaMaps maps, const MlaArgs a) {
     using namespace mla;
+    using L = Layout<NS>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
     const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
-    const uint32_t bar0 = smem_addr(bars);
+    const uint32_t bar0 = smem_addr(smem + L::kOffBars);
     auto bar = [bar0](int i) { return bar0 + 8u * (uint32_t)i; };
-    volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
+    auto kv_full = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + s); };
+    auto kv_empty = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + NS + s); };
+    volatile int* misc = reinterpret_cast<volatile int*>(smem + L::kOffMisc);
     volatile int* abort_word = misc + 1;
-    int* scratch = reinterpret_cast<int*>(smem + kOffScratch);
-    int* cum = reinterpret_cast<int*>(smem + kOffCum);
-    const uint32_t sKV = smem_addr(smem + kOffKV);
+    int* scratch = reinterpret_cast<int*>(smem + L::kOffRecv);   // free until the first exchange
+    int* cum = reinterpret_cast<int*>(smem + L::kOffCum);
+    const uint32_t sKV = smem_addr(smem + L::kOffKV);
+    const uint32_t sQR = smem_addr(smem + L::kOffQR);
 
     if (tid == 0) {
-        mbar_init(bar(B_Q_FULL), kSoftWarps);
-        mbar_init(bar(B_Q_FREE), 1);
-        for (int s = 0; s < kNS; ++s) {
-            mbar_init(bar(B_KV_FULL + s), 1);
-            mbar_init(bar(B_KV_EMPTY + s), 1);
-        }
-        mbar_init(bar(B_S_FULL), 1);
-        mbar_init(bar(B_S_FREE), kSoftWarps);
-        mbar_init(bar(B_P_FULL), kSoftWarps);
-        mbar_init(bar(B_P_FREE), 1);
-        mbar_init(bar(B_O_FREE), kSoftWarps);
+        mbar_init(bar(B_Q_FULL), kSoftWarps);    // each group loads half of every Q
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(B_RECV_FULL + i), 1);           // expect_tx by the receiver
-            mbar_init(bar(B_RECV_EMPTY + i), kSoftWarps); // remote arrivals of the peer's warps
+            mbar_init(bar(B_S_FULL + i), 1);
+            mbar_init(bar(B_P_FULL + i), kGroupWarps);
+            mbar_init(bar(B_PV_DONE + i), 1);
+            mbar_init(bar(B_RECV_FULL + i), 1);             // expect_tx by the receiver
+            mbar_init(bar(B_RECV_EMPTY + i), kGroupWarps);  // remote arrivals of the peer's group
         }
-        for (int q = 0; q < 4; ++q) mbar_init(bar(B_PAIR + q), 2);
+        mbar_init(bar(B_O_FREE), kGroupWarps);
+        for (int i = 0; i < 16; ++i) mbar_init(bar(B_HAND + i), 1);
         mbar_init(bar(B_DONE), 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(kv_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+        }
         misc[1] = 0;
         fence_barrier_init();
     }
     if (warp == kSoftWarps) {
-        tmem_alloc(smem_addr(smem + kOffMisc), kTmemCols);
+        tmem_alloc(smem_addr(smem + L::kOffMisc), kTmemCols);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -133,10 +141,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     const int w = pair;
     const long long t_begin = (w < S.W && S.T > 0) ? S.item_begin(w) : 0;
     const long long t_end = (w < S.W && S.T > 0) ? S.item_begin(w + 1) : 0;
+    const long long n = t_end - t_begin;   // pages of this pair, local index j in [0, n)
 
     if (warp == kSoftWarps + 1) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && t_begin < t_end) {
+        if (lane == 0 && n > 0) {
             const uint64_t pol = l2_policy_evict_first();
             prefetch_tensormap(&maps.c128);
             prefetch_tensormap(&maps.c64);
@@ -153,406 +162,430 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                            : -1;
             };
             int page = page_of(cur);
-            for (long long t = t_begin; t < t_end; ++t) {
-                if (!wait_or_abort(bar(B_KV_EMPTY + stage), phase ^ 1, abort_word, a.err, a.timeout_ns)) break;
+            for (long long j = 0; j < n; ++j) {
+                if (!wait_or_abort(kv_empty(stage), phase ^ 1, abort_word, a.err, a.timeout_ns)) break;
                 if (page < 0 || page >= a.num_pages) {
                     report(a.err, KVDEC_DEVERR_BAD_PAGE);
                     page = 0;
                 }
-                const uint32_t fb = bar(B_KV_FULL + stage);
+                const uint32_t fb = kv_full(stage);
                 const uint32_t dst = sKV + stage * kStageBytes;
                 mbar_arrive_expect_tx(fb, kStageBytes);
                 for (int c = 0; c < 4; ++c)
                     tma_load_2d(dst + c * 8192, &maps.c128, fb, 256 * rank + 64 * c, page * kTileTokens, pol);
                 tma_load_2d(dst + 32768, &maps.c64, fb, 512 + 32 * rank, page * kTileTokens, pol);
                 ++issued;
-                if (++stage == kNS) {
+                if (++stage == NS) {
                     stage = 0;
                     phase ^= 1;
                 }
                 cur.advance(S);
                 // fetch the next page index now, so its latency overlaps the next wait
-                if (t + 1 < t_end) page = page_of(cur);
+                if (j + 1 < n) page = page_of(cur);
             }
             // never leave TMA writes in flight
-            for (long long i = (issued > kNS ? issued - kNS : 0); i < issued; ++i)
-                if (!mbar_wait_bounded(bar(B_KV_FULL + (int)(i % kNS)), (uint32_t)((i / kNS) & 1), a.timeout_ns)) {
+            for (long long i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+                if (!mbar_wait_bounded(kv_full((int)(i % NS)), (uint32_t)((i / NS) & 1), a.timeout_ns)) {
                     report(a.err, KVDEC_DEVERR_TIMEOUT);
                     break;
                 }
         }
     } else if (warp == kSoftWarps) {
         // ------------------------------------------------------------ MMA issuer
-        // Issues S(next) as soon as its page, its Q and a free S buffer are
-        // there (at most two pages ahead of PV), and PV(next) as soon as its
-        // P is in TMEM; never blocks on one while the other could go.
-        if (lane == 0 && t_begin < t_end) {
+        // Fixed order: S(0), S(1), then for every page j: PV(j) once P(j) is
+        // in TMEM, and S(j+2) into the same buffer once PV(j), the last reader
+        // of that buffer's P, has completed (or after PV(j+1), see below).  Blocking waits park the thread
+        // (no polling that would take issue slots from the softmax warps).
+        if (lane == 0 && n > 0) {
             constexpr uint32_t iS = umma_idesc_bf16(128, 64, false, false);
             constexpr uint32_t iP = umma_idesc_bf16(128, 256, false, true);
-            const long long n = t_end - t_begin;
             TileCursor cs;                       // page of the next S
             cs.start(S, t_begin);
-            long long ns = 0, np = 0;            // next S / next PV page index
             int seg_s = -1;                      // segment of the last issued S
             int ring_seg[4];
             bool ring_first[4];
-            uint64_t t_wait = 0;
-            bool stuck = false;
-            while (np < n) {
-                bool progress = false;
-                if (ns < n && ns <= np + 2) {
-                    const bool first = (ns == 0) || cs.lt == 0;
-                    const bool last = (cs.lt == cs.nt - 1) || (ns == n - 1);
-                    const int stage = (int)(ns % kNS);
-                    const bool ready =
-                        (!first || mbar_try_wait(bar(B_Q_FULL), (uint32_t)((seg_s + 1) & 1))) &&
-                        mbar_try_wait(bar(B_KV_FULL + stage), (uint32_t)((ns / kNS) & 1)) &&
-                        (ns == 0 || mbar_try_wait(bar(B_S_FREE), (uint32_t)((ns - 1) & 1)));
-                    if (ready) {
-                        if (first) ++seg_s;
-                        tc_fence_after();
-                        const uint32_t kb = sKV + stage * kStageBytes;
-                        for (int q = 0; q < 16; ++q)
-                            umma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + 8 * q,
-                                         umma_desc(kb + (q >> 2) * 8192 + (q & 3) * 32, 16, 1024, kSwizzle128B),
-                                         iS, q > 0);
-                        for (int q = 0; q < 2; ++q)
-                            umma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + 128 + 8 * q,
-                                         umma_desc(kb + 32768 + q * 32, 16, 512, kSwizzle64B), iS, 1u);
-                        umma_commit(bar(B_S_FULL));
-                        if (last) umma_commit(bar(B_Q_FREE));
-                        ring_seg[ns & 3] = seg_s;
-                        ring_first[ns & 3] = first;
-                        ++ns;
-                        cs.advance(S);
-                        progress = true;
-                    }
+            auto issue_s = [&](long long j) -> bool {
+                const bool first = (j == 0) || cs.lt == 0;
+                if (first) {
+                    ++seg_s;
+                    if (!wait_or_abort(bar(B_Q_FULL), (uint32_t)(seg_s & 1), abort_word, a.err, a.timeout_ns))
+                        return false;
                 }
-                if (np < ns) {
-                    const bool pfirst = ring_first[np & 3];
-                    const int pseg = ring_seg[np & 3];
-                    const bool ready =
-                        mbar_try_wait(bar(B_P_FULL), (uint32_t)(np & 1)) &&
-                        (!pfirst || pseg == 0 || mbar_try_wait(bar(B_O_FREE), (uint32_t)((pseg - 1) & 1)));
-                    if (ready) {
-                        tc_fence_after();
-                        const int pst = (int)(np % kNS);
-                        const uint32_t vb = sKV + pst * kStageBytes;
-                        for (int ks = 0; ks < 4; ++ks)
-                            umma_bf16_ts(tmem + kTmemO, tmem + kTmemP + 8 * ks,
-                                         umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
-                                         (pfirst && ks == 0) ? 0u : 1u);
-                        umma_commit(bar(B_P_FREE));
-                        umma_commit(bar(B_KV_EMPTY + pst));
-                        ++np;
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    t_wait = 0;
-                } else {
-                    if (*abort_word) break;
-                    const uint64_t now = global_timer_ns();
-                    if (t_wait == 0) {
-                        t_wait = now;
-                    } else if (now - t_wait > a.timeout_ns) {
-                        stuck = true;
-                        break;
-                    }
-                }
+                const int stage = (int)(j % NS);
+                const int sb = (int)(j & 1);
+                if (!wait_or_abort(kv_full(stage), (uint32_t)((j / NS) & 1), abort_word, a.err, a.timeout_ns))
+                    return false;
+                if (j >= 2 && !wait_or_abort(bar(B_PV_DONE + sb), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
+                                             a.timeout_ns))
+                    return false;
+                tc_fence_after();
+                const uint32_t kb = sKV + stage * kStageBytes;
+                const uint32_t d = tmem + kTmemS + 64u * sb;
+                for (int q = 0; q < 16; ++q)
+                    umma_bf16_ts(d, tmem + kTmemQ + 8 * q,
+                                 umma_desc(kb + (q >> 2) * 8192 + (q & 3) * 32, 16, 1024, kSwizzle128B), iS, q > 0);
+                for (int q = 0; q < 2; ++q)
+                    umma_bf16_ss(d, umma_desc(sQR + q * 32, 16, 512, kSwizzle64B),
+                                 umma_desc(kb + 32768 + q * 32, 16, 512, kSwizzle64B), iS, 1u);
+                umma_commit(bar(B_S_FULL + sb));
+                ring_seg[j & 3] = seg_s;
+                ring_first[j & 3] = first;
+                cs.advance(S);
+                return true;
+            };
+            // An S that starts a sequence needs that sequence's Q, which is only
+            // loaded after P of the page before it: such an S waits until that
+            // page's PV has been issued (`defer`), so that its flush is not held up.
+            bool ok = issue_s(0), defer = false;
+            if (ok && n >= 2) {
+                if (cs.lt == 0) defer = true;
+                else ok = issue_s(1);
             }
-            if (stuck) {
-                *abort_word = 1;
-                report(a.err, KVDEC_DEVERR_TIMEOUT);
+            for (long long j = 0; ok && j < n; ++j) {
+                const bool pfirst = ring_first[j & 3];
+                const int pseg = ring_seg[j & 3];
+                const int pb = (int)(j & 1);
+                if (!wait_or_abort(bar(B_P_FULL + pb), (uint32_t)((j >> 1) & 1), abort_word, a.err, a.timeout_ns))
+                    break;
+                if (pfirst && pseg > 0 &&
+                    !wait_or_abort(bar(B_O_FREE), (uint32_t)((pseg - 1) & 1), abort_word, a.err, a.timeout_ns))
+                    break;
+                tc_fence_after();
+                const int pst = (int)(j % NS);
+                const uint32_t vb = sKV + pst * kStageBytes;
+                for (int ks = 0; ks < 4; ++ks)
+                    umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + 64u * pb + 8 * ks,
+                                 umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
+                                 (pfirst && ks == 0) ? 0u : 1u);
+                umma_commit(bar(B_PV_DONE + pb));
+                umma_commit(kv_empty(pst));
+                if (defer) {
+                    defer = false;
+                    if (!(ok = issue_s(j + 1))) break;
+                }
+                if (j + 2 < n) {
+                    if (cs.lt == 0) defer = true;
+                    else ok = issue_s(j + 2);
+                }
             }
             // every MMA issued by this thread has completed before TMEM is freed
             umma_commit(bar(B_DONE));
             if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps
-        const int qd = warp & 3, half = warp >> 2;
-        const int row = qd * 32 + lane;                       // head = TMEM lane
+        // ------------------------------------------------------------ softmax groups
+        // Group g takes the pages j with j % 2 == g; thread (qd, lane) of a
+        // group owns head row = 32 qd + lane, i.e. TMEM lane `row`.
+        const int g = warp >> 2, qd = warp & 3;
+        const int row = qd * 32 + lane;
+        const int gtid = tid & 127;
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-        const uint4* recv4 = reinterpret_cast<const uint4*>(smem + kOffRecv);    // [2][8][128]
-        float* red = reinterpret_cast<float*>(smem + kOffRed);       // [2][2][128]
-        float* red_l = reinterpret_cast<float*>(smem + kOffRedL);    // [2][128]
-        const uint32_t peer_recv = mapa_shared(smem_addr(smem + kOffRecv), peer);
-        const uint32_t peer_full = mapa_shared(bar(B_RECV_FULL), peer);
-        const uint32_t peer_empty = mapa_shared(bar(B_RECV_EMPTY), peer);
-        const uint32_t pair_bar = bar(B_PAIR + qd);
+        const uint32_t tS = trow + kTmemS + 64u * (uint32_t)g;   // this group's S / P buffer
+        const uint4* recv4 = reinterpret_cast<const uint4*>(smem + L::kOffRecv + g * kRecvBytes);  // [8][128]
+        float2* hand = reinterpret_cast<float2*>(smem + L::kOffHand);                             // [2][2][128]
+        const uint32_t peer_recv = mapa_shared(smem_addr(smem + L::kOffRecv + g * kRecvBytes), peer);
+        const uint32_t peer_full = mapa_shared(bar(B_RECV_FULL + g), peer);
+        const uint32_t peer_empty = mapa_shared(bar(B_RECV_EMPTY + g), peer);
         const float sl2 = a.scale_log2;
-        uint32_t pair_uses = 0;
-        // row-wide exchange with the other half of this quadrant
-        auto pair_sync = [&]() -> bool {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(pair_bar);
-            const bool ok = wait_or_abort(pair_bar, pair_uses & 1, abort_word, a.err, a.timeout_ns);
-            ++pair_uses;
-            return ok;
-        };
+        uint32_t hand_waits[2] = {0u, 0u};
 
         // sequences with no tokens
         for (int b = 0; b < a.B; ++b) {
             if (w >= S.W || S.ntiles(b) != 0 || b % S.W != w) continue;
-            const size_t base = ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * half;
+            const size_t base = ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * g;
             for (int c = 0; c < 128; c += 4) {
                 if (a.out_bf16)
                     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + base + c) = make_uint2(0u, 0u);
                 else
                     *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + base + c) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            if (rank == 0 && half == 0 && a.lse) a.lse[(size_t)b * kHeads + row] = -INFINITY;
+            if (rank == 0 && g == 0 && a.lse) a.lse[(size_t)b * kHeads + row] = -INFINITY;
         }
 
-        const long long n = t_end - t_begin;
-        int qseg = -1;
-        // Q_r of a sequence -> TMEM (bf16 pairs), once the previous sequence's
-        // last S has completed
-        auto load_q = [&](int b) -> bool {
-            ++qseg;
-            if (qseg > 0 &&
-                !wait_or_abort(bar(B_Q_FREE), (uint32_t)((qseg - 1) & 1), abort_word, a.err, a.timeout_ns))
-                return false;
-            const uint4* qa_row = reinterpret_cast<const uint4*>(
-                a.q_abs + ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * half);
-            uint32_t v[16];
+        // Q_r of sequence b, this group's half: latent dims [128 g, 128 g + 128)
+        // -> TMEM (bf16 pairs), rope dims [16 g, 16 g + 16) -> shared memory,
+        // K-major with the 64-byte swizzle (16-byte chunk c of row r stored at
+        // chunk c ^ ((r >> 1) & 3)).  Called once the previous sequence's last
+        // S has completed.
+        auto load_q = [&](int b) {
+            const uint4* qa = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * g);
+            const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + ((size_t)b * kHeads + row) * 64 + 32 * rank);
+            uint4 x[16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {       // 128 bf16 of q_abs = 64 columns
-                const uint4 x0 = __ldg(qa_row + 4 * c), x1 = __ldg(qa_row + 4 * c + 1);
-                const uint4 x2 = __ldg(qa_row + 4 * c + 2), x3 = __ldg(qa_row + 4 * c + 3);
-                v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-                v[8] = x2.x; v[9] = x2.y; v[10] = x2.z; v[11] = x2.w;
-                v[12] = x3.x; v[13] = x3.y; v[14] = x3.z; v[15] = x3.w;
-                tmem_st16u(trow + kTmemQ + 64 * half + 16 * c, v);
-            }
-            if (half == 1) {                    // 32 bf16 of q_rope = 16 columns
-                const uint4* qr_row = reinterpret_cast<const uint4*>(
-                    a.q_rope + ((size_t)b * kHeads + row) * 64 + 32 * rank);
-                const uint4 x0 = __ldg(qr_row), x1 = __ldg(qr_row + 1);
-                const uint4 x2 = __ldg(qr_row + 2), x3 = __ldg(qr_row + 3);
-                v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-                v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-                v[8] = x2.x; v[9] = x2.y; v[10] = x2.z; v[11] = x2.w;
-                v[12] = x3.x; v[13] = x3.y; v[14] = x3.z; v[15] = x3.w;
-                tmem_st16u(trow + kTmemQ + 128, v);
+            for (int i = 0; i < 16; ++i) x[i] = __ldg(qa + i);
+#pragma unroll
+            for (int c = 2 * g; c < 2 * g + 2; ++c)
+                *reinterpret_cast<uint4*>(smem + L::kOffQR + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = __ldg(qr + c);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t v[16];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    v[4 * k] = x[4 * c + k].x;
+                    v[4 * k + 1] = x[4 * c + k].y;
+                    v[4 * k + 2] = x[4 * c + k].z;
+                    v[4 * k + 3] = x[4 * c + k].w;
+                }
+                tmem_st16u(trow + kTmemQ + 64 * g + 16 * c, v);
             }
             tmem_st_wait();
+            fence_proxy_async();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(B_Q_FULL));
-            return true;
-        };
-        // partial S of page j (this half's 32 columns) -> registers and, with
-        // asynchronous remote stores, the peer's receive buffer j & 1
-        auto read_send = [&](long long j, float (&dst)[32]) -> bool {
-            if (!wait_or_abort(bar(B_S_FULL), (uint32_t)(j & 1), abort_word, a.err, a.timeout_ns)) return false;
-            tc_fence_after();
-            tmem_ld16(trow + kTmemS + 32 * half, *reinterpret_cast<float(*)[16]>(dst));
-            tmem_ld16(trow + kTmemS + 32 * half + 16, *reinterpret_cast<float(*)[16]>(dst + 16));
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_S_FREE));
-            const uint32_t buf = (uint32_t)(j & 1);
-            if (j >= 2 && !wait_cluster_or_abort(bar(B_RECV_EMPTY + (int)buf), (uint32_t)(((j - 2) >> 1) & 1),
-                                                 abort_word, a.err, a.timeout_ns))
-                return false;
-            // sent as fp16: the error this adds to a probability is relative,
-            // about scale * |S_peer| * 2^-12, no larger than the bf16 rounding of P
-            const uint32_t dst_base = peer_recv + buf * kRecvBytes;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                uint4 hv;
-                hv.x = pack_half2(dst[8 * k], dst[8 * k + 1]);
-                hv.y = pack_half2(dst[8 * k + 2], dst[8 * k + 3]);
-                hv.z = pack_half2(dst[8 * k + 4], dst[8 * k + 5]);
-                hv.w = pack_half2(dst[8 * k + 6], dst[8 * k + 7]);
-                st_async_u4(dst_base + (uint32_t)(((4 * half + k) * kHeads + row) * 16), hv, peer_full + 8u * buf);
-            }
-            return true;
         };
 
-        TileCursor cur, nxt;
-        float s_cur[32], s_nxt[32];
-        bool ok = true;
+        TileCursor cur;
+        long long seg_start = 0;     // first page of the current segment (one sequence's pages)
+        int lt0 = 0;                 // tile index of page 0 inside its sequence
         if (n > 0) {
             cur.start(S, t_begin);
-            nxt = cur;
-            ok = load_q(cur.b) && read_send(0, s_cur);
-        }
-        float m_run = -INFINITY, l_run = 0.f;
-        int len = 0;
-        bool seg_item_first = true, seg_unit_first = true;
-        for (long long it = 0; ok && it < n; ++it) {
-            const long long t = t_begin + it;
-            const bool seg_first = (t == t_begin) || cur.lt == 0;
-            const bool seg_last = (cur.lt == cur.nt - 1) || (t == t_end - 1);
-            // ---- look ahead: the next page's partial S leaves for the peer now
-            if (it + 1 < n) {
-                nxt.advance(S);
-                if (nxt.lt == 0 && !load_q(nxt.b)) break;
-                if (!read_send(it + 1, s_nxt)) break;
+            lt0 = cur.lt;
+            load_q(cur.b);
+            if (g == 1 && n > 1) {
+                cur.advance(S);
+                if (cur.lt == 0) seg_start = 1;
             }
-            if (seg_first) {
-                // warm L2 with the next sequence's Q rows, needed at the next switch
-                if (cur.b + 1 < a.B) {
-                    const char* nq = reinterpret_cast<const char*>(
-                        a.q_abs + ((size_t)(cur.b + 1) * kHeads + row) * 512 + 256 * rank + 128 * half);
-                    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(nq));
-                    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(nq + 128));
-                    if (half == 1)
-                        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<const char*>(
-                            a.q_rope + ((size_t)(cur.b + 1) * kHeads + row) * 64 + 32 * rank)));
-                }
-                m_run = -INFINITY;
-                l_run = 0.f;
+        }
+        float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
+        int len = 0;
+        for (long long j = g; j < n; j += 2) {
+            const bool seg_first = (seg_start == j);
+            const bool seg_last = (cur.lt == cur.nt - 1) || (j == n - 1);
+            // page j + 1 ends the segment: its group needs this group's row sum
+            const bool pre_last = !seg_last && ((cur.lt + 1 == cur.nt - 1) || (j + 1 == n - 1));
+            if (seg_start >= j - 1) {     // this group's first page of the segment
+                m_g = -INFINITY;
+                l_g = 0.f;
                 len = clamp_len(__ldg(a.seqlens + cur.b), cap, nullptr);
-                seg_item_first = (t == t_begin);
-                seg_unit_first = (cur.lt == 0);
+            }
+            if (seg_first && cur.b + 1 < a.B) {
+                // warm L2 with the next sequence's Q rows, loaded at the next switch
+                const char* nq = reinterpret_cast<const char*>(a.q_abs + ((size_t)(cur.b + 1) * kHeads + row) * 512 + 256 * rank);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(nq + 128 * c));
+                asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(reinterpret_cast<const char*>(
+                    a.q_rope + ((size_t)(cur.b + 1) * kHeads + row) * 64 + 32 * rank)));
+            }
+            if (seg_first && j > 0) {
+                // this group's half of the new Q, once S(j-1), the last S of the
+                // previous sequence, has completed (the other group loads its half
+                // after reading that S)
+                if (!wait_or_abort(bar(B_S_FULL + (g ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word, a.err,
+                                   a.timeout_ns))
+                    break;
+                tc_fence_after();
+                load_q(cur.b);
             }
             const int n_valid = min(kTileTokens, len - cur.lt * kTileTokens);
-            // ---- the peer's partial S of this page
-            const int buf = (int)(it & 1);
-            if (tid == 0) mbar_arrive_expect_tx(bar(B_RECV_FULL + buf), kRecvBytes);
-            if (!wait_cluster_or_abort(bar(B_RECV_FULL + buf), (uint32_t)((it >> 1) & 1), abort_word, a.err,
-                                       a.timeout_ns))
-                break;
-            float s[32];
+            const uint32_t u = (uint32_t)(j >> 1);   // use index of this group's buffers
+
+            // ---- this CTA's partial S(j) -> registers
+            if (!wait_or_abort(bar(B_S_FULL + g), u & 1, abort_word, a.err, a.timeout_ns)) break;
+            tc_fence_after();
+            float s[64];
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 x = recv4[(buf * 8 + 4 * half + k) * kHeads + row];
+            for (int c = 0; c < 4; ++c) tmem_ld16(tS + 16 * c, *reinterpret_cast<float(*)[16]>(s + 16 * c));
+            tmem_ld_wait();
+            // ---- ... and to the peer as fp16 (asynchronous remote stores that
+            // complete on the peer's barrier).  The error this adds to a
+            // probability is relative, about scale * |S_peer| * 2^-12, no larger
+            // than the bf16 rounding of P.
+            if (u >= 1 && !wait_cluster_or_abort(bar(B_RECV_EMPTY + g), (u - 1) & 1, abort_word, a.err, a.timeout_ns))
+                break;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                uint4 hv;
+                hv.x = pack_half2(s[8 * k], s[8 * k + 1]);
+                hv.y = pack_half2(s[8 * k + 2], s[8 * k + 3]);
+                hv.z = pack_half2(s[8 * k + 4], s[8 * k + 5]);
+                hv.w = pack_half2(s[8 * k + 6], s[8 * k + 7]);
+                st_async_u4(peer_recv + (uint32_t)((k * kHeads + row) * 16), hv, peer_full);
+            }
+            // ---- the peer's partial
+            if (gtid == 0) mbar_arrive_expect_tx(bar(B_RECV_FULL + g), kRecvBytes);
+            if (!wait_cluster_or_abort(bar(B_RECV_FULL + g), u & 1, abort_word, a.err, a.timeout_ns)) break;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const uint4 x = recv4[k * kHeads + row];
                 const float2 a0 = unpack_half2(x.x), a1 = unpack_half2(x.y);
                 const float2 a2 = unpack_half2(x.z), a3 = unpack_half2(x.w);
-                s[8 * k] = s_cur[8 * k] + a0.x;
-                s[8 * k + 1] = s_cur[8 * k + 1] + a0.y;
-                s[8 * k + 2] = s_cur[8 * k + 2] + a1.x;
-                s[8 * k + 3] = s_cur[8 * k + 3] + a1.y;
-                s[8 * k + 4] = s_cur[8 * k + 4] + a2.x;
-                s[8 * k + 5] = s_cur[8 * k + 5] + a2.y;
-                s[8 * k + 6] = s_cur[8 * k + 6] + a3.x;
-                s[8 * k + 7] = s_cur[8 * k + 7] + a3.y;
+                s[8 * k] += a0.x;
+                s[8 * k + 1] += a0.y;
+                s[8 * k + 2] += a1.x;
+                s[8 * k + 3] += a1.y;
+                s[8 * k + 4] += a2.x;
+                s[8 * k + 5] += a2.y;
+                s[8 * k + 6] += a3.x;
+                s[8 * k + 7] += a3.y;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(peer_empty + 8u * (uint32_t)buf);
-            // ---- row max over both halves, lazy rescale, base-2 probabilities
+            // the buffer goes back to the peer now, or after the flush, which
+            // stages through it
+            if (!seg_last) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster_relaxed(peer_empty);
+            }
+            // ---- row max of this page (scale > 0)
             float mx = -INFINITY;
 #pragma unroll
-            for (int j2 = 0; j2 < 32; ++j2) {
-                if (32 * half + j2 >= n_valid) s[j2] = -INFINITY;
-                mx = fmaxf(mx, s[j2]);
+            for (int i = 0; i < 64; ++i) {
+                if (i >= n_valid) s[i] = -INFINITY;
+                mx = fmaxf(mx, s[i]);
             }
-            red[((it & 1) * 2 + half) * kHeads + row] = mx;
-            if (!pair_sync()) break;
-            mx = fmaxf(mx, red[((it & 1) * 2 + (half ^ 1)) * kHeads + row]) * sl2;
-            float alpha = 1.f;
+            mx *= sl2;
+            // ---- running max after page j - 1, from the other group
+            float m_prev = -INFINITY, l_o = 0.f;
+            if (!seg_first) {
+                const int k = (int)(((j - 1) >> 1) & 1);
+                if (!wait_or_abort(bar(B_HAND + (qd * 2 + (g ^ 1)) * 2 + k), hand_waits[k] & 1, abort_word, a.err,
+                                   a.timeout_ns))
+                    break;
+                ++hand_waits[k];
+                const float2 h = hand[((g ^ 1) * 2 + k) * kHeads + row];
+                m_prev = h.x;
+                l_o = h.y;
+            }
+            // lazy rescale: the reference max moves only when a row's max
+            // exceeds it by more than 2^8
+            float m_new = m_prev, alpha = 1.f;
             bool resc = false;
-            if (mx > m_run + 8.f) {
-                resc = (m_run != -INFINITY);
-                alpha = resc ? fast_exp2(m_run - mx) : 0.f;
-                m_run = mx;
+            if (mx > m_prev + 8.f) {
+                resc = !seg_first;
+                alpha = resc ? fast_exp2(m_prev - mx) : 0.f;
+                m_new = mx;
             }
+            const int kp = (int)((j >> 1) & 1);
+            float2* hout = hand + (g * 2 + kp) * kHeads + row;
+            const uint32_t hbar = bar(B_HAND + (qd * 2 + g) * 2 + kp);
+            if (!seg_last && !pre_last) {     // page j + 1 only needs the max: hand it over now
+                *hout = make_float2(m_new, 0.f);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar);
+            }
+            // ---- probabilities (base 2) -> P in TMEM over the first 32 columns of S
             float lsum = 0.f;
-            uint32_t pk[16];
 #pragma unroll
-            for (int j2 = 0; j2 < 16; ++j2) {
-                const float p0 = fast_exp2(fmaf(s[2 * j2], sl2, -m_run));
-                const float p1 = fast_exp2(fmaf(s[2 * j2 + 1], sl2, -m_run));
-                lsum += p0 + p1;
-                pk[j2] = pack_bf16x2(p0, p1);
+            for (int c = 0; c < 2; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float p0 = fast_exp2(fmaf(s[32 * c + 2 * i], sl2, -m_new));
+                    const float p1 = fast_exp2(fmaf(s[32 * c + 2 * i + 1], sl2, -m_new));
+                    lsum += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                tmem_st16u(tS + 16 * c, pk);
             }
-            l_run = l_run * alpha + lsum;      // this half's share of the row sum
-            // ---- P (this half's 32 tokens) -> TMEM once PV of the previous page is done
-            if (it > 0 &&
-                !wait_or_abort(bar(B_P_FREE), (uint32_t)((it - 1) & 1), abort_word, a.err, a.timeout_ns))
-                break;
-            tc_fence_after();
-            tmem_st16u(trow + kTmemP + 16 * half, pk);
-            // ---- tail page: zero the unused V rows (stale bytes may be NaN)
+            l_g = l_g * fast_exp2(m_g - m_new) + lsum;
+            m_g = m_new;
+            if (pre_last) {
+                *hout = make_float2(m_new, l_g);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar);
+            }
+            // ---- rescale O where the running max moved (rare): after PV(j-1), before PV(j)
+            if (__any_sync(0xffffffffu, resc)) {
+                if (!wait_or_abort(bar(B_PV_DONE + (g ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word, a.err,
+                                   a.timeout_ns))
+                    break;
+                tc_fence_after();
+                for (int c0 = 0; c0 < 256; c0 += 16) {
+                    float o[16];
+                    tmem_ld16(trow + kTmemO + c0, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= alpha;
+                    tmem_st16(trow + kTmemO + c0, o);
+                }
+            }
+            // ---- tail page: zero the V rows past the sequence end (stale bytes may be NaN)
             if (n_valid < kTileTokens) {
-                uint8_t* st = smem + kOffKV + (int)(it % kNS) * kStageBytes;
+                uint8_t* st = smem + L::kOffKV + (int)(j % NS) * kStageBytes;
                 const int nz = (kTileTokens - n_valid) * 32;   // 16-byte chunks over 4 boxes
-                for (int i2 = tid; i2 < nz; i2 += 32 * kSoftWarps) {
-                    const int r = n_valid + (i2 >> 5), bx = (i2 >> 3) & 3, ch = i2 & 7;
+                for (int i = gtid; i < nz; i += 32 * kGroupWarps) {
+                    const int r = n_valid + (i >> 5), bx = (i >> 3) & 3, ch = i & 7;
                     *reinterpret_cast<uint4*>(st + bx * 8192 + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 fence_proxy_async();
             }
-            // ---- rescale this half's 128 O columns where the running max moved (rare)
-            if (!seg_first && __any_sync(0xffffffffu, resc)) {
-                for (int c0 = 0; c0 < 128; c0 += 16) {
-                    float o[16];
-                    tmem_ld16(trow + kTmemO + 128 * half + c0, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2) o[i2] *= alpha;
-                    tmem_st16(trow + kTmemO + 128 * half + c0, o);
-                }
-            }
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_P_FULL));
+            if (lane == 0) mbar_arrive(bar(B_P_FULL + g));
 
             if (seg_last) {
-                // ---------------------------------------------------- flush
-                red_l[half * kHeads + row] = l_run;
-                if (!pair_sync()) break;
-                const float l_tot = l_run + red_l[(half ^ 1) * kHeads + row];
-                if (!wait_or_abort(bar(B_P_FREE), (uint32_t)(it & 1), abort_word, a.err, a.timeout_ns)) break;
+                // the next sequence's Q: S(j) was the last reader of the current one
+                if (j + 1 < n) {
+                    TileCursor nx = cur;
+                    nx.advance(S);
+                    load_q(nx.b);
+                }
+                // ------------------------------------------------------ flush
+                const float l_tot = l_g + (seg_first ? 0.f : l_o * fast_exp2(m_prev - m_new));
+                if (!wait_or_abort(bar(B_PV_DONE + g), u & 1, abort_word, a.err, a.timeout_ns)) break;
                 tc_fence_after();
-                const bool complete = seg_unit_first && (cur.lt == cur.nt - 1);
-                const int slot = 2 * w + (seg_item_first ? 0 : 1);
+                const bool complete = (seg_start > 0 || lt0 == 0) && (cur.lt == cur.nt - 1);
+                const int slot = 2 * w + (seg_start == 0 ? 0 : 1);
                 const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
-                const float lse_v = l_tot > 0.f ? (m_run + __log2f(l_tot)) * kLn2 : -INFINITY;
+                const float lse_v = l_tot > 0.f ? (m_new + __log2f(l_tot)) * kLn2 : -INFINITY;
                 const size_t orow = (size_t)cur.b * kHeads + row;
-                const int col0 = 256 * (int)rank + 128 * half;
-                float* pdst = a.part_o + ((size_t)slot * kHeads + row) * 512 + col0;
-                for (int c0 = 0; c0 < 128; c0 += 16) {
-                    float o[16];
-                    tmem_ld16(trow + kTmemO + 128 * half + c0, o);
+                const int col0 = 256 * (int)rank;
+                // O / l goes out 32 columns at a time through this warp's quarter
+                // of the group's exchange buffer (32 rows x 128 B; chunk c of row
+                // r at chunk c ^ (r & 7)), so that every store writes whole lines:
+                // lane (r8, ch) writes 16-byte chunk ch of rows r8, r8 + 4, ...
+                float* stg = reinterpret_cast<float*>(smem + L::kOffRecv + g * kRecvBytes + qd * 4096);
+                const int r8 = lane >> 3, ch = lane & 7;
+                const size_t drow0 = complete ? (size_t)cur.b * kHeads + qd * 32 : (size_t)slot * kHeads + qd * 32;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    float o[32];
+                    tmem_ld16(trow + kTmemO + c0, *reinterpret_cast<float(*)[16]>(o));
+                    tmem_ld16(trow + kTmemO + c0 + 16, *reinterpret_cast<float(*)[16]>(o + 16));
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i2 = 0; i2 < 16; ++i2) o[i2] *= inv;
-                    if (!complete) {
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4*>(stg + lane * 32 + ((c ^ (lane & 7)) << 2)) =
+                            make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
+                    __syncwarp();
 #pragma unroll
-                        for (int i2 = 0; i2 < 16; i2 += 4)
-                            *reinterpret_cast<float4*>(pdst + c0 + i2) = make_float4(o[i2], o[i2 + 1], o[i2 + 2], o[i2 + 3]);
-                    } else if (a.out_bf16) {
-                        __nv_bfloat16* d = reinterpret_cast<__nv_bfloat16*>(a.out) + orow * 512 + col0 + c0;
-#pragma unroll
-                        for (int i2 = 0; i2 < 16; i2 += 8)
-                            *reinterpret_cast<uint4*>(d + i2) =
-                                make_uint4(pack_bf16x2(o[i2], o[i2 + 1]), pack_bf16x2(o[i2 + 2], o[i2 + 3]),
-                                           pack_bf16x2(o[i2 + 4], o[i2 + 5]), pack_bf16x2(o[i2 + 6], o[i2 + 7]));
-                    } else {
-                        float* d = reinterpret_cast<float*>(a.out) + orow * 512 + col0 + c0;
-#pragma unroll
-                        for (int i2 = 0; i2 < 16; i2 += 4)
-                            *reinterpret_cast<float4*>(d + i2) = make_float4(o[i2], o[i2 + 1], o[i2 + 2], o[i2 + 3]);
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = 4 * k + r8;
+                        const float4 v = *reinterpret_cast<const float4*>(stg + r * 32 + ((ch ^ (r & 7)) << 2));
+                        const size_t off = (drow0 + r) * 512 + col0 + c0 + 4 * ch;
+                        if (!complete)
+                            *reinterpret_cast<float4*>(a.part_o + off) = v;
+                        else if (a.out_bf16)
+                            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
+                                make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+                        else
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = v;
                     }
+                    __syncwarp();
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_O_FREE));
+                if (lane == 0) {
+                    mbar_arrive(bar(B_O_FREE));
+                    mbar_arrive_cluster_relaxed(peer_empty);   // staging reads are done
+                }
                 if (complete) {
-                    if (rank == 0 && half == 0 && a.lse) a.lse[orow] = lse_v;
+                    if (rank == 0 && a.lse) a.lse[orow] = lse_v;
                 } else {
-                    // this warp's own copy of the partial lse: [rank][half][slot][row]
-                    float* plse = a.part_lse + (size_t)(rank * 2 + half) * (2 * npairs) * kHeads;
+                    // this CTA's copy of the partial lse: [rank][slot][row]
+                    float* plse = a.part_lse + (size_t)rank * (2 * npairs) * kHeads;
                     plse[(size_t)slot * kHeads + row] = lse_v;
                     __threadfence();
                     __syncwarp();
                     int last = 0;
                     if (lane == 0)
-                        last = arrive_piece(a.counters + ((size_t)cur.b * 2 + rank) * kSoftWarps + warp, a.epoch,
+                        last = arrive_piece(a.counters + ((size_t)cur.b * 2 + rank) * 4 + qd, a.epoch,
                                             (uint32_t)S.num_pieces(cur.b, 0))
                                    ? 1
                                    : 0;
                     last = __shfl_sync(0xffffffffu, last, 0);
                     if (last) {
-                        // merge this warp's 32 heads x 128 columns over every piece
+                        // merge this warp's 32 heads x 256 columns over every piece
                         __threadfence();
                         const int npc = S.num_pieces(cur.b, 0);
                         int w0, kind0;
@@ -567,47 +600,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                             const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
                             den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
                         }
-                        if (rank == 0 && half == 0 && a.lse) a.lse[orow] = den > 0.f ? M + __logf(den) : -INFINITY;
+                        if (rank == 0 && a.lse) a.lse[orow] = den > 0.f ? M + __logf(den) : -INFINITY;
                         const float invd = den > 0.f ? 1.f / den : 0.f;
-                        // 8 rows at a time, every row's load in flight together
-                        for (int r0 = 0; r0 < 32; r0 += 8) {
+                        // 8 rows x 128 columns at a time, every row's load in flight together
+                        for (int r0 = 0; r0 < 64; r0 += 8) {
+                            const int rr = r0 & 31, ch = r0 >> 5;
                             float4 acc[8];
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
                             for (int s2 = 0; s2 < npc; ++s2) {
                                 const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
                                 const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
                                 const float wm = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * invd;
                                 const float4* src = reinterpret_cast<const float4*>(
-                                    a.part_o + ((size_t)sl * kHeads + qd * 32 + r0) * 512 + col0) + lane;
-                                float4 v[8];
+                                    a.part_o + ((size_t)sl * kHeads + qd * 32 + rr) * 512 + col0 + 128 * ch) + lane;
+                                float4 x[8];
 #pragma unroll
-                                for (int u = 0; u < 8; ++u) v[u] = __ldcg(src + (size_t)u * 128);
+                                for (int v = 0; v < 8; ++v) x[v] = __ldcg(src + (size_t)v * 128);
 #pragma unroll
-                                for (int u = 0; u < 8; ++u) {
-                                    const float wgt = __shfl_sync(0xffffffffu, wm, r0 + u);
-                                    acc[u].x = fmaf(wgt, v[u].x, acc[u].x);
-                                    acc[u].y = fmaf(wgt, v[u].y, acc[u].y);
-                                    acc[u].z = fmaf(wgt, v[u].z, acc[u].z);
-                                    acc[u].w = fmaf(wgt, v[u].w, acc[u].w);
+                                for (int v = 0; v < 8; ++v) {
+                                    const float wgt = __shfl_sync(0xffffffffu, wm, rr + v);
+                                    acc[v].x = fmaf(wgt, x[v].x, acc[v].x);
+                                    acc[v].y = fmaf(wgt, x[v].y, acc[v].y);
+                                    acc[v].z = fmaf(wgt, x[v].z, acc[v].z);
+                                    acc[v].w = fmaf(wgt, x[v].w, acc[v].w);
                                 }
                             }
 #pragma unroll
-                            for (int u = 0; u < 8; ++u) {
-                                const size_t off = ((size_t)cur.b * kHeads + qd * 32 + r0 + u) * 512 + col0 + 4 * lane;
+                            for (int v = 0; v < 8; ++v) {
+                                const size_t off =
+                                    ((size_t)cur.b * kHeads + qd * 32 + rr + v) * 512 + col0 + 128 * ch + 4 * lane;
                                 if (a.out_bf16)
                                     *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
-                                        make_uint2(pack_bf16x2(acc[u].x, acc[u].y), pack_bf16x2(acc[u].z, acc[u].w));
+                                        make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
                                 else
-                                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[u];
+                                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[v];
                             }
                         }
                     }
                 }
             }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) s_cur[k] = s_nxt[k];
-            cur.advance(S);
+            // ---- the other group's page, then this group's next page
+            for (long long k2 = 1; k2 <= 2 && j + k2 < n; ++k2) {
+                cur.advance(S);
+                if (cur.lt == 0) seg_start = j + k2;
+            }
         }
     }
 
@@ -622,17 +659,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     cluster_sync_all();   // the peer no longer touches this CTA's shared memory
 }
 
-cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    const int smem = mla::smem_bytes(a.B);
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+namespace {
+int optin_smem() {
+    int dev = 0, v = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) return 0;
+    return v;
+}
+
+// five cache stages when they fit beside the batch's tile table, else four
+bool five_stages(int B) { return mla::Layout<5>::smem_bytes(B) <= optin_smem(); }
+
+template <int NS>
+cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
+    const int smem = mla::Layout<NS>::smem_bytes(a.B);
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    mla_decode_kernel<<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
+    mla_decode_kernel<NS><<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
-int max_pairs_mla(int B) {
-    const int smem = mla::smem_bytes(B);
-    if (cudaFuncSetAttribute(mla_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+template <int NS>
+int max_pairs_ns(int B) {
+    const int smem = mla::Layout<NS>::smem_bytes(B);
+    if (cudaFuncSetAttribute(mla_decode_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -649,8 +699,15 @@ int max_pairs_mla(int B) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<NS>, &cfg) != cudaSuccess) return 0;
     return n;
 }
+}  // namespace
+
+cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
+    return five_stages(a.B) ? launch_ns<5>(maps, a, pairs, st) : launch_ns<4>(maps, a, pairs, st);
+}
+
+int max_pairs_mla(int B) { return five_stages(B) ? max_pairs_ns<5>(B) : max_pairs_ns<4>(B); }
 
 }  // namespace kvdec

@@ -86,7 +86,8 @@ typedef enum kvdec_dtype { KVDEC_F32 = 0, KVDEC_BF16 = 1 } kvdec_dtype;
  *   out    [batch, num_heads, head_dim], F32 or BF16 (out_dtype)
  *   lse    fp32 [batch, num_heads] or NULL
  * Supported: head_dim in {64, 128}; num_heads % num_kv_heads == 0;
- * q, k, v, out 16-byte aligned.  scale == 0 selects 1/sqrt(head_dim).
+ * q, k, v, out 16-byte aligned.  scale == 0 selects 1/sqrt(head_dim); any other
+ * scale must be positive and finite (KVDEC_ERR_INVALID_ARG otherwise).
  * Workspace: at least kvdec_gqa_workspace_bytes(p) bytes, 256-byte aligned,
  * no initialisation needed (split counters are tagged with a per-call epoch).
  * It holds the split partials and their counters; calls that share it must
@@ -159,7 +160,8 @@ kvdec_status kvdec_gqa_decode_noalloc(const kvdec_gqa_params* p, void* stream);
  *   s_j  = scale * (q_absorbed[b,h,:] . c_kv_j + q_rope[b,h,:] . k_R_j)
  *   out[b,h,:] = sum_j softmax(s)_j c_kv_j        (latent space, 512 wide)
  * V is the first 512 values of the same row.  scale == 0 selects
- * 1/sqrt(128 + 64) = 1/sqrt(192), the pre-absorption head dim.
+ * 1/sqrt(128 + 64) = 1/sqrt(192), the pre-absorption head dim; any other
+ * scale must be positive and finite (KVDEC_ERR_INVALID_ARG otherwise).
  * W_UK (folded into q_absorbed) and W_UV / W_O (applied to out) are the
  * caller's.
  *

@@ -67,3 +67,10 @@ def test_host_rejects_bad_arguments(cuda_lib):
     q96 = torch.zeros(1, 8, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(KvdecError, match="head_dim 96"):
         cuda_lib.gqa_decode(q96, k96, k96, case.seqlens)
+    for bad in (-0.5, float("nan"), float("inf")):
+        with pytest.raises(KvdecError, match="scale"):
+            cuda_lib.gqa_decode(case.q, case.k, case.v, case.seqlens, scale=bad)
+    mc = kvgen.mla_case(1, 128, seqlens=[70], seed=47, device="cuda")
+    with pytest.raises(KvdecError, match="scale"):
+        cuda_lib.mla_decode_absorbed(mc.q_abs, mc.q_rope, mc.cache, mc.block_table, mc.seqlens,
+                                     scale=-0.1)

@@ -127,3 +127,26 @@ def test_bad_page_reported(cuda_lib):
     torch.cuda.synchronize()
     assert flag.item() & cuda_lib.DEVERR_BAD_PAGE
     assert torch.isfinite(out).all()
+
+
+@pytest.mark.parametrize("max_ctas", [2, 0])
+def test_lazy_rescale_heavy_tail(cuda_lib, max_ctas):
+    """Heavy-tailed rope scores (logits up to ~20): row maxima jump by more
+    than 2^8 at random pages of both parities, so O is rescaled mid-sequence
+    by both softmax groups; one pair (max_ctas=2) walks every page."""
+    case = kvgen.mla_case(2, 128, seqlens=[3000, 1100], seed=218, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(9)
+    case.q_rope.zero_()
+    case.q_rope[:, :, 0] = (1.5 * torch.randn((2, 128), generator=g, device="cuda")).to(torch.bfloat16)
+    spikes = torch.empty(case.cache.shape[:2], device="cuda").exponential_(1.0, generator=g)
+    case.cache[:, :, 512] = (12.0 * spikes).to(torch.bfloat16)
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas)
+    ref, lref = full_oracle(case)
+    # the rope part of the scores alone already moves some row maxima by
+    # more than 8 (log2 units) after the first page
+    t = torch.arange(3000)
+    k0 = case.cache.cpu().double()[case.block_table.cpu()[0, t // 64].long(), t % 64, 512]
+    sc = case.q_rope.cpu().double()[0, :, :1] * k0[None, :] * case.scale / np.log(2)
+    assert ((sc.max(1).values - sc[:, :64].max(1).values) > 8.0).any()
+    assert_attn_close(out, ref, f"heavy tail, max_ctas={max_ctas}")
+    assert_lse_close(lse, lref)

@@ -21,21 +21,23 @@
 // cache byte is read from HBM once and no MMA is duplicated.
 //   TMEM per CTA (512 columns): O_r [0,256), the 256 latent dims of Q_r
 //   [256,384) (bf16 pairs), and two S buffers [384,448), [448,512), one per
-//   softmax group; P (bf16 pairs) overwrites the first 32 columns of its S.
-//   The 32 rope dims of Q_r sit in shared memory (8 KB), beside five (four
-//   for very large batches) 36 KB cache stages (TMA, 128/64-byte swizzle)
-//   and two 16 KB exchange buffers.
+//   softmax group.  Shared memory: five (four for very large batches)
+//   36 KB cache stages (TMA, 128/64-byte swizzle), a 16 KB exchange buffer
+//   and a 16 KB P buffer, each taken by the pages in turn (PV reads P from
+//   shared memory, so an S buffer is free again as soon as its softmax has
+//   loaded it), and the 32 rope dims of Q_r (8 KB).
 // The partial S travels to the peer as fp16 with asynchronous remote stores
 // that complete on the peer's mbarrier; with two groups, one page's exchange
-// overlaps the other page's softmax.  The MMA thread keeps S up to two pages
-// ahead of PV.
+// overlaps the other page's softmax.  S runs up to two pages ahead of PV,
+// so the next page's S is ready when a group finishes a page.
 // Roles: warps 0-7 run the softmax in two groups of four that take
 // alternate pages (ping-pong); in a group, thread i owns head i (TMEM lane i)
 // and all 64 columns of the page.  Only the running max and the running sum
 // pass from one group to the other, through a small hand-off buffer.  Warp 8
-// issues the MMAs (one thread) and owns the TMEM allocation; warp 9 issues
-// the TMA loads (one thread).  Softmax is base 2 with lazy rescaling: O is
-// rescaled only when a row's running max grows by more than 2^8.
+// issues the S MMAs (one thread) and owns the TMEM allocation; warp 9 issues
+// the TMA loads (one thread), warp 10 the PV MMAs (one thread).
+// Softmax is base 2 with lazy rescaling: O is rescaled only when a row's
+// running max grows by more than 2^8.
 // The split-KV schedule (schedule.cuh) gives each CTA pair an equal share of
 // all pages; sequences cut across pairs leave normalised partials, merged by
 // log-sum-exp ([ARG] §五.2) by the last piece to finish, per warp tile.
@@ -50,29 +52,32 @@ namespace mla {
 constexpr int kHeads = 128;
 constexpr int kStageBytes = 4 * 8192 + 4096;    // c_kv 4 x [64 x 64] SW128 + rope [64 x 32] SW64
 constexpr int kRecvBytes = 8 * kHeads * 16;     // one exchange buffer: [8][128] uint4 (8 fp16)
+constexpr int kPBytes = kHeads * 128;           // P [128 x 64] bf16, K-major SW128
 constexpr int kQRBytes = kHeads * 64;           // q_rope [128 x 32] bf16, K-major SW64
 constexpr int kHandBytes = 2 * 2 * kHeads * 8;  // hand-off: [2 groups][2][128] (m, l)
 constexpr int kSoftWarps = 8;                   // two groups of four
 constexpr int kGroupWarps = 4;
-constexpr int kThreads = 32 * (kSoftWarps + 2);
+constexpr int kThreads = 32 * (kSoftWarps + 3);   // + S issuer, TMA producer, PV issuer
 enum {
-    B_Q_FULL, B_S_FULL, B_P_FULL = B_S_FULL + 2, B_PV_DONE = B_P_FULL + 2, B_O_FREE = B_PV_DONE + 2,
-    B_RECV_FULL, B_RECV_EMPTY = B_RECV_FULL + 2, B_HAND = B_RECV_EMPTY + 2,   // [4 quadrants][2 groups][2]
+    B_Q_FULL, B_S_FULL, B_S_FREE = B_S_FULL + 2, B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2,
+    B_O_FREE = B_PV_DONE + 2, B_RECV_FULL, B_RECV_EMPTY,
+    B_HAND,                                                                    // [4 quadrants][2 groups][2]
     B_DONE = B_HAND + 16, B_KV = B_DONE + 1                                    // then full[NS], empty[NS]
 };
 template <int NS>
 struct Layout {
     static constexpr int kOffKV = 0;
     static constexpr int kOffRecv = NS * kStageBytes;
-    static constexpr int kOffQR = kOffRecv + 2 * kRecvBytes;
+    static constexpr int kOffP = kOffRecv + kRecvBytes;
+    static constexpr int kOffQR = kOffP + kPBytes;
     static constexpr int kOffHand = kOffQR + kQRBytes;
     static constexpr int kOffBars = kOffHand + kHandBytes;
     static constexpr int kBars = B_KV + 2 * NS;
     static constexpr int kOffMisc = kOffBars + ((kBars * 8 + 15) & ~15);   // [0] TMEM base, [1] abort word
     static constexpr int kOffCum = kOffMisc + 16;
     static constexpr int smem_bytes(int B) { return kOffCum + (B + 1) * 4 + 1024; }
-    static_assert(kOffRecv % 1024 == 0 && kOffQR % 1024 == 0, "alignment");
-    static_assert(kThreads * 4 <= 2 * kRecvBytes, "scan scratch lives in the exchange buffers");
+    static_assert(kOffRecv % 1024 == 0 && kOffP % 1024 == 0 && kOffQR % 1024 == 0, "alignment");
+    static_assert(kThreads * 4 <= kRecvBytes, "scan scratch lives in the exchange buffer");
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -101,19 +106,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     int* cum = reinterpret_cast<int*>(smem + L::kOffCum);
     const uint32_t sKV = smem_addr(smem + L::kOffKV);
     const uint32_t sQR = smem_addr(smem + L::kOffQR);
+    const uint32_t sP = smem_addr(smem + L::kOffP);
 
     if (tid == 0) {
         mbar_init(bar(B_Q_FULL), kSoftWarps);    // each group loads half of every Q
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_S_FULL + i), 1);
+            mbar_init(bar(B_S_FREE + i), kGroupWarps);
             mbar_init(bar(B_P_FULL + i), kGroupWarps);
             mbar_init(bar(B_PV_DONE + i), 1);
-            mbar_init(bar(B_RECV_FULL + i), 1);             // expect_tx by the receiver
-            mbar_init(bar(B_RECV_EMPTY + i), kGroupWarps);  // remote arrivals of the peer's group
         }
+        mbar_init(bar(B_RECV_FULL), 1);             // expect_tx by the receiver
+        mbar_init(bar(B_RECV_EMPTY), kGroupWarps);  // remote arrivals of the peer's reading group
         mbar_init(bar(B_O_FREE), kGroupWarps);
         for (int i = 0; i < 16; ++i) mbar_init(bar(B_HAND + i), 1);
-        mbar_init(bar(B_DONE), 1);
+        mbar_init(bar(B_DONE), 2);                  // both MMA issuers
         for (int s = 0; s < NS; ++s) {
             mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
@@ -128,10 +135,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     }
     const int cap = a.max_blocks * kTileTokens;
     build_cum(cum, scratch, a.seqlens, a.B, cap, a.err);   // ends with __syncthreads
-    tc_fence_after();
-    cluster_sync_all();                                    // the peer's barriers exist
-    const uint32_t tmem = (uint32_t)misc[0];
-
     TileSchedule S;
     S.cum = cum;
     S.B = a.B;
@@ -142,6 +145,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     const long long t_begin = (w < S.W && S.T > 0) ? S.item_begin(w) : 0;
     const long long t_end = (w < S.W && S.T > 0) ? S.item_begin(w + 1) : 0;
     const long long n = t_end - t_begin;   // pages of this pair, local index j in [0, n)
+    // the exchange buffer's phase j holds the peer's partial S of page j; the
+    // reader of page j registers the bytes of page j + 1
+    if (tid == 0 && n > 0) mbar_arrive_expect_tx(bar(B_RECV_FULL), kRecvBytes);
+    tc_fence_after();
+    cluster_sync_all();                                    // the peer's barriers exist
+    const uint32_t tmem = (uint32_t)misc[0];
 
     if (warp == kSoftWarps + 1) {
         // ------------------------------------------------------------ producer
@@ -191,33 +200,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 }
         }
     } else if (warp == kSoftWarps) {
-        // ------------------------------------------------------------ MMA issuer
-        // Fixed order: S(0), S(1), then for every page j: PV(j) once P(j) is
-        // in TMEM, and S(j+2) into the same buffer once PV(j), the last reader
-        // of that buffer's P, has completed (or after PV(j+1), see below).  Blocking waits park the thread
-        // (no polling that would take issue slots from the softmax warps).
+        // ------------------------------------------------------------ S issuer
+        // S(j) goes to TMEM buffer j & 1 once its page and Q are there and the
+        // softmax has read S(j-2) out of that buffer.  PV has its own issuer
+        // (the last warp), so that a PV never queues behind a later S.
+        // Blocking waits park the thread.
         if (lane == 0 && n > 0) {
             constexpr uint32_t iS = umma_idesc_bf16(128, 64, false, false);
-            constexpr uint32_t iP = umma_idesc_bf16(128, 256, false, true);
-            TileCursor cs;                       // page of the next S
+            TileCursor cs;
             cs.start(S, t_begin);
-            int seg_s = -1;                      // segment of the last issued S
-            int ring_seg[4];
-            bool ring_first[4];
-            auto issue_s = [&](long long j) -> bool {
-                const bool first = (j == 0) || cs.lt == 0;
-                if (first) {
-                    ++seg_s;
-                    if (!wait_or_abort(bar(B_Q_FULL), (uint32_t)(seg_s & 1), abort_word, a.err, a.timeout_ns))
-                        return false;
-                }
+            uint32_t seg_s = 0;                  // sequences started so far
+            for (long long j = 0; j < n; ++j) {
+                if ((j == 0 || cs.lt == 0) &&
+                    !wait_or_abort(bar(B_Q_FULL), (seg_s++) & 1u, abort_word, a.err, a.timeout_ns))
+                    break;
                 const int stage = (int)(j % NS);
                 const int sb = (int)(j & 1);
-                if (!wait_or_abort(kv_full(stage), (uint32_t)((j / NS) & 1), abort_word, a.err, a.timeout_ns))
-                    return false;
-                if (j >= 2 && !wait_or_abort(bar(B_PV_DONE + sb), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
+                if (!wait_or_abort(kv_full(stage), (uint32_t)((j / NS) & 1), abort_word, a.err, a.timeout_ns)) break;
+                if (j >= 2 && !wait_or_abort(bar(B_S_FREE + sb), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
                                              a.timeout_ns))
-                    return false;
+                    break;
                 tc_fence_after();
                 const uint32_t kb = sKV + stage * kStageBytes;
                 const uint32_t d = tmem + kTmemS + 64u * sb;
@@ -228,47 +230,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     umma_bf16_ss(d, umma_desc(sQR + q * 32, 16, 512, kSwizzle64B),
                                  umma_desc(kb + 32768 + q * 32, 16, 512, kSwizzle64B), iS, 1u);
                 umma_commit(bar(B_S_FULL + sb));
-                ring_seg[j & 3] = seg_s;
-                ring_first[j & 3] = first;
                 cs.advance(S);
-                return true;
-            };
-            // An S that starts a sequence needs that sequence's Q, which is only
-            // loaded after P of the page before it: such an S waits until that
-            // page's PV has been issued (`defer`), so that its flush is not held up.
-            bool ok = issue_s(0), defer = false;
-            if (ok && n >= 2) {
-                if (cs.lt == 0) defer = true;
-                else ok = issue_s(1);
             }
-            for (long long j = 0; ok && j < n; ++j) {
-                const bool pfirst = ring_first[j & 3];
-                const int pseg = ring_seg[j & 3];
+            // every MMA issued by this thread has completed before TMEM is freed
+            umma_commit(bar(B_DONE));
+            if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+        }
+    } else if (warp == kSoftWarps + 2) {
+        // ------------------------------------------------------------ PV issuer
+        // PV(j) once P(j) is in shared memory (and, at a sequence's first page,
+        // once the previous sequence's O has been flushed); then the page's
+        // stage goes back to the producer.
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t iP = umma_idesc_bf16(128, 256, false, true);
+            TileCursor cp;
+            cp.start(S, t_begin);
+            uint32_t seg_p = 0;                  // sequences started so far
+            for (long long j = 0; j < n; ++j) {
+                const bool first = (j == 0) || cp.lt == 0;
+                if (first) ++seg_p;
                 const int pb = (int)(j & 1);
                 if (!wait_or_abort(bar(B_P_FULL + pb), (uint32_t)((j >> 1) & 1), abort_word, a.err, a.timeout_ns))
                     break;
-                if (pfirst && pseg > 0 &&
-                    !wait_or_abort(bar(B_O_FREE), (uint32_t)((pseg - 1) & 1), abort_word, a.err, a.timeout_ns))
+                if (first && seg_p > 1 &&
+                    !wait_or_abort(bar(B_O_FREE), (seg_p - 2) & 1u, abort_word, a.err, a.timeout_ns))
                     break;
                 tc_fence_after();
                 const int pst = (int)(j % NS);
                 const uint32_t vb = sKV + pst * kStageBytes;
                 for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16_ts(tmem + kTmemO, tmem + kTmemS + 64u * pb + 8 * ks,
+                    umma_bf16_ss(tmem + kTmemO, umma_desc(sP + ks * 32, 16, 1024, kSwizzle128B),
                                  umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
-                                 (pfirst && ks == 0) ? 0u : 1u);
+                                 (first && ks == 0) ? 0u : 1u);
                 umma_commit(bar(B_PV_DONE + pb));
                 umma_commit(kv_empty(pst));
-                if (defer) {
-                    defer = false;
-                    if (!(ok = issue_s(j + 1))) break;
-                }
-                if (j + 2 < n) {
-                    if (cs.lt == 0) defer = true;
-                    else ok = issue_s(j + 2);
-                }
+                cp.advance(S);
             }
-            // every MMA issued by this thread has completed before TMEM is freed
             umma_commit(bar(B_DONE));
             if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
@@ -280,12 +277,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         const int row = qd * 32 + lane;
         const int gtid = tid & 127;
         const uint32_t trow = tmem + ((uint32_t)(qd * 32) << 16);
-        const uint32_t tS = trow + kTmemS + 64u * (uint32_t)g;   // this group's S / P buffer
-        const uint4* recv4 = reinterpret_cast<const uint4*>(smem + L::kOffRecv + g * kRecvBytes);  // [8][128]
-        float2* hand = reinterpret_cast<float2*>(smem + L::kOffHand);                             // [2][2][128]
-        const uint32_t peer_recv = mapa_shared(smem_addr(smem + L::kOffRecv + g * kRecvBytes), peer);
-        const uint32_t peer_full = mapa_shared(bar(B_RECV_FULL + g), peer);
-        const uint32_t peer_empty = mapa_shared(bar(B_RECV_EMPTY + g), peer);
+        const uint32_t tS = trow + kTmemS + 64u * (uint32_t)g;   // this group's S buffer
+        const uint4* recv4 = reinterpret_cast<const uint4*>(smem + L::kOffRecv);   // [8][128]
+        float2* hand = reinterpret_cast<float2*>(smem + L::kOffHand);              // [2][2][128]
+        const uint32_t peer_recv = mapa_shared(smem_addr(smem + L::kOffRecv), peer);
+        const uint32_t peer_full = mapa_shared(bar(B_RECV_FULL), peer);
+        const uint32_t peer_empty = mapa_shared(bar(B_RECV_EMPTY), peer);
         const float sl2 = a.scale_log2;
         uint32_t hand_waits[2] = {0u, 0u};
 
@@ -337,6 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
 
         TileCursor cur;
         long long seg_start = 0;     // first page of the current segment (one sequence's pages)
+        int seg_idx = 0;             // index of that segment among the pair's segments
         int lt0 = 0;                 // tile index of page 0 inside its sequence
         if (n > 0) {
             cur.start(S, t_begin);
@@ -344,7 +342,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             load_q(cur.b);
             if (g == 1 && n > 1) {
                 cur.advance(S);
-                if (cur.lt == 0) seg_start = 1;
+                if (cur.lt == 0) {
+                    seg_start = 1;
+                    ++seg_idx;
+                }
             }
         }
         float m_g = -INFINITY, l_g = 0.f;   // this group's share of the row sum, relative to m_g
@@ -387,11 +388,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld16(tS + 16 * c, *reinterpret_cast<float(*)[16]>(s + 16 * c));
             tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(B_S_FREE + g));   // S(j+2) may go into this buffer
             // ---- ... and to the peer as fp16 (asynchronous remote stores that
             // complete on the peer's barrier).  The error this adds to a
             // probability is relative, about scale * |S_peer| * 2^-12, no larger
             // than the bf16 rounding of P.
-            if (u >= 1 && !wait_cluster_or_abort(bar(B_RECV_EMPTY + g), (u - 1) & 1, abort_word, a.err, a.timeout_ns))
+            if (j >= 1 && !wait_cluster_or_abort(bar(B_RECV_EMPTY), (uint32_t)((j - 1) & 1), abort_word, a.err,
+                                                 a.timeout_ns))
                 break;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -403,8 +408,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 st_async_u4(peer_recv + (uint32_t)((k * kHeads + row) * 16), hv, peer_full);
             }
             // ---- the peer's partial
-            if (gtid == 0) mbar_arrive_expect_tx(bar(B_RECV_FULL + g), kRecvBytes);
-            if (!wait_cluster_or_abort(bar(B_RECV_FULL + g), u & 1, abort_word, a.err, a.timeout_ns)) break;
+            if (!wait_cluster_or_abort(bar(B_RECV_FULL), (uint32_t)(j & 1), abort_word, a.err, a.timeout_ns)) break;
+            if (gtid == 0 && j + 1 < n) mbar_arrive_expect_tx(bar(B_RECV_FULL), kRecvBytes);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const uint4 x = recv4[k * kHeads + row];
@@ -419,12 +424,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 s[8 * k + 6] += a3.x;
                 s[8 * k + 7] += a3.y;
             }
-            // the buffer goes back to the peer now, or after the flush, which
-            // stages through it
-            if (!seg_last) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster_relaxed(peer_empty);
-            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster_relaxed(peer_empty);
             // ---- row max of this page (scale > 0)
             float mx = -INFINITY;
 #pragma unroll
@@ -462,19 +463,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(hbar);
             }
-            // ---- probabilities (base 2) -> P in TMEM over the first 32 columns of S
+            // ---- probabilities (base 2) -> P(j) in shared memory, K-major with the
+            // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)),
+            // once PV(j-1) has read the buffer (at a sequence's first page: once
+            // the previous sequence's flush, which stages through it, is done)
+            if (seg_first && j > 0) {
+                if (!wait_or_abort(bar(B_O_FREE), (uint32_t)((seg_idx - 1) & 1), abort_word, a.err, a.timeout_ns))
+                    break;
+            } else if (j >= 1 && !wait_or_abort(bar(B_PV_DONE + (g ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word,
+                                                a.err, a.timeout_ns)) {
+                break;
+            }
+            uint8_t* prow = smem + L::kOffP + row * 128;
             float lsum = 0.f;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t pk[16];
+            for (int c = 0; c < 8; ++c) {
+                uint32_t pk[4];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float p0 = fast_exp2(fmaf(s[32 * c + 2 * i], sl2, -m_new));
-                    const float p1 = fast_exp2(fmaf(s[32 * c + 2 * i + 1], sl2, -m_new));
+                for (int i = 0; i < 4; ++i) {
+                    const float p0 = fast_exp2(fmaf(s[8 * c + 2 * i], sl2, -m_new));
+                    const float p1 = fast_exp2(fmaf(s[8 * c + 2 * i + 1], sl2, -m_new));
                     lsum += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
-                tmem_st16u(tS + 16 * c, pk);
+                *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
             l_g = l_g * fast_exp2(m_g - m_new) + lsum;
             m_g = m_new;
@@ -506,8 +518,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                     const int r = n_valid + (i >> 5), bx = (i >> 3) & 3, ch = i & 7;
                     *reinterpret_cast<uint4*>(st + bx * 8192 + r * 128 + ch * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
-                fence_proxy_async();
             }
+            fence_proxy_async();   // P and the zeroed rows -> the tensor cores
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -531,10 +543,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 const size_t orow = (size_t)cur.b * kHeads + row;
                 const int col0 = 256 * (int)rank;
                 // O / l goes out 32 columns at a time through this warp's quarter
-                // of the group's exchange buffer (32 rows x 128 B; chunk c of row
-                // r at chunk c ^ (r & 7)), so that every store writes whole lines:
-                // lane (r8, ch) writes 16-byte chunk ch of rows r8, r8 + 4, ...
-                float* stg = reinterpret_cast<float*>(smem + L::kOffRecv + g * kRecvBytes + qd * 4096);
+                // of the P buffer (32 rows x 128 B; chunk c of row r at chunk
+                // c ^ (r & 7)), so that every store writes whole lines: lane
+                // (r8, ch) writes 16-byte chunk ch of rows r8, r8 + 4, ...  PV(j)
+                // has read P(j); the next P waits for O_FREE.
+                float* stg = reinterpret_cast<float*>(smem + L::kOffP + qd * 4096);
                 const int r8 = lane >> 3, ch = lane & 7;
                 const size_t drow0 = complete ? (size_t)cur.b * kHeads + qd * 32 : (size_t)slot * kHeads + qd * 32;
 #pragma unroll 1
@@ -565,10 +578,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(bar(B_O_FREE));
-                    mbar_arrive_cluster_relaxed(peer_empty);   // staging reads are done
-                }
+                if (lane == 0) mbar_arrive(bar(B_O_FREE));
                 if (complete) {
                     if (rank == 0 && a.lse) a.lse[orow] = lse_v;
                 } else {
@@ -643,7 +653,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             // ---- the other group's page, then this group's next page
             for (long long k2 = 1; k2 <= 2 && j + k2 < n; ++k2) {
                 cur.advance(S);
-                if (cur.lt == 0) seg_start = j + k2;
+                if (cur.lt == 0) {
+                    seg_start = j + k2;
+                    ++seg_idx;
+                }
             }
         }
     }

@@ -29,6 +29,14 @@ KVDEC_DEVINL uint64_t global_timer_ns() {
     return t;
 }
 
+// True once more than timeout_ns have passed since t0.  The global timer is
+// not guaranteed to be monotonic (it may be stepped), so a reading below t0
+// counts as no time passed rather than wrapping around to a huge interval.
+KVDEC_DEVINL bool timed_out(uint64_t t0, uint64_t timeout_ns) {
+    const uint64_t now = global_timer_ns();
+    return now > t0 && now - t0 > timeout_ns;
+}
+
 KVDEC_DEVINL void report(uint32_t* flag, uint32_t bits) {
     if (flag) atomicOr(flag, bits);
 }
@@ -87,7 +95,7 @@ KVDEC_DEVINL bool mbar_wait_bounded(uint32_t bar, uint32_t parity, uint64_t time
 #pragma unroll 1
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > timeout_ns) return false;
+        if (timed_out(t0, timeout_ns)) return false;
     }
 }
 
@@ -105,7 +113,7 @@ KVDEC_DEVINL bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abo
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (*abort_word) return false;
-        if (global_timer_ns() - t0 > timeout_ns) {
+        if (timed_out(t0, timeout_ns)) {
             *abort_word = 1;
             report(err, KVDEC_DEVERR_TIMEOUT);
             return false;
@@ -189,7 +197,7 @@ KVDEC_DEVINL bool wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile 
         for (int i = 0; i < 32; ++i)
             if (mbar_try_wait_acq_cluster(bar, parity)) return true;
         if (*abort_word) return false;
-        if (global_timer_ns() - t0 > timeout_ns) {
+        if (timed_out(t0, timeout_ns)) {
             *abort_word = 1;
             report(err, KVDEC_DEVERR_TIMEOUT);
             return false;

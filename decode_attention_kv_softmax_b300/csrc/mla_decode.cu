@@ -64,12 +64,12 @@ enum {
     B_HAND,                                                                    // [4 quadrants][2 groups][2]
     B_DONE = B_HAND + 16, B_KV = B_DONE + 1                                    // then full[NS], empty[NS]
 };
-template <int NS>
+template <int NS, int PB>
 struct Layout {
     static constexpr int kOffKV = 0;
     static constexpr int kOffRecv = NS * kStageBytes;
     static constexpr int kOffP = kOffRecv + kRecvBytes;
-    static constexpr int kOffQR = kOffP + kPBytes;
+    static constexpr int kOffQR = kOffP + PB * kPBytes;
     static constexpr int kOffHand = kOffQR + kQRBytes;
     static constexpr int kOffBars = kOffHand + kHandBytes;
     static constexpr int kBars = B_KV + 2 * NS;
@@ -85,11 +85,11 @@ constexpr uint32_t kTmemQ = 256;
 constexpr uint32_t kTmemS = 384;
 }  // namespace mla
 
-template <int NS>
+template <int NS, int PB>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ MlaMaps maps, const MlaArgs a) {
     using namespace mla;
-    using L = Layout<NS>;
+    using L = Layout<NS, PB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -259,7 +259,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 const int pst = (int)(j % NS);
                 const uint32_t vb = sKV + pst * kStageBytes;
                 for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16_ss(tmem + kTmemO, umma_desc(sP + ks * 32, 16, 1024, kSwizzle128B),
+                    umma_bf16_ss(tmem + kTmemO, umma_desc(sP + (PB == 2 ? pb * kPBytes : 0) + ks * 32, 16, 1024, kSwizzle128B),
                                  umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
                                  (first && ks == 0) ? 0u : 1u);
                 umma_commit(bar(B_PV_DONE + pb));
@@ -424,16 +424,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 s[8 * k + 6] += a3.x;
                 s[8 * k + 7] += a3.y;
             }
+            // the buffer may take the peer's next page (none after the last: no
+            // remote operation is left in flight when the CTAs exit)
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster_relaxed(peer_empty);
-            // ---- row max of this page (scale > 0)
-            float mx = -INFINITY;
+            if (lane == 0 && j + 1 < n) mbar_arrive_cluster_relaxed(peer_empty);
+            // ---- row max of this page (scale > 0), as a tree
+            if (n_valid < kTileTokens) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                if (i >= n_valid) s[i] = -INFINITY;
-                mx = fmaxf(mx, s[i]);
+                for (int i = 0; i < 64; ++i)
+                    if (i >= n_valid) s[i] = -INFINITY;
             }
-            mx *= sl2;
+            float mt[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mt[i] = fmaxf(s[i], s[i + 32]);
+#pragma unroll
+            for (int w2 = 16; w2 >= 1; w2 >>= 1)
+#pragma unroll
+                for (int i = 0; i < w2; ++i) mt[i] = fmaxf(mt[i], mt[i + w2]);
+            const float mx = mt[0] * sl2;
             // ---- running max after page j - 1, from the other group
             float m_prev = -INFINITY, l_o = 0.f;
             if (!seg_first) {
@@ -467,15 +475,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)),
             // once PV(j-1) has read the buffer (at a sequence's first page: once
             // the previous sequence's flush, which stages through it, is done)
-            if (seg_first && j > 0) {
+            if (PB == 2) {
+                if (j >= 2 && !wait_or_abort(bar(B_PV_DONE + g), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
+                                             a.timeout_ns))
+                    break;
+            } else if (seg_first && j > 0) {
                 if (!wait_or_abort(bar(B_O_FREE), (uint32_t)((seg_idx - 1) & 1), abort_word, a.err, a.timeout_ns))
                     break;
             } else if (j >= 1 && !wait_or_abort(bar(B_PV_DONE + (g ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word,
                                                 a.err, a.timeout_ns)) {
                 break;
             }
-            uint8_t* prow = smem + L::kOffP + row * 128;
-            float lsum = 0.f;
+            uint8_t* prow = smem + L::kOffP + (PB == 2 ? g * kPBytes : 0) + row * 128;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
                 uint32_t pk[4];
@@ -483,11 +495,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 for (int i = 0; i < 4; ++i) {
                     const float p0 = fast_exp2(fmaf(s[8 * c + 2 * i], sl2, -m_new));
                     const float p1 = fast_exp2(fmaf(s[8 * c + 2 * i + 1], sl2, -m_new));
-                    lsum += p0 + p1;
+                    ls[i] += p0 + p1;
                     pk[i] = pack_bf16x2(p0, p1);
                 }
                 *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_g = l_g * fast_exp2(m_g - m_new) + lsum;
             m_g = m_new;
             if (pre_last) {
@@ -547,7 +560,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 // c ^ (r & 7)), so that every store writes whole lines: lane
                 // (r8, ch) writes 16-byte chunk ch of rows r8, r8 + 4, ...  PV(j)
                 // has read P(j); the next P waits for O_FREE.
-                float* stg = reinterpret_cast<float*>(smem + L::kOffP + qd * 4096);
+                float* stg = reinterpret_cast<float*>(smem + L::kOffP + (PB == 2 ? g * kPBytes : 0) + qd * 4096);
                 const int r8 = lane >> 3, ch = lane & 7;
                 const size_t drow0 = complete ? (size_t)cur.b * kHeads + qd * 32 : (size_t)slot * kHeads + qd * 32;
 #pragma unroll 1
@@ -669,6 +682,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");   // this thread's remote operations are done
     cluster_sync_all();   // the peer no longer touches this CTA's shared memory
 }
 
@@ -680,22 +694,27 @@ int optin_smem() {
     return v;
 }
 
-// five cache stages when they fit beside the batch's tile table, else four
-bool five_stages(int B) { return mla::Layout<5>::smem_bytes(B) <= optin_smem(); }
+#ifndef KVDEC_MLA_NS
+#define KVDEC_MLA_NS 5
+#define KVDEC_MLA_PB 1
+#endif
+// the preferred configuration when it fits beside the batch's tile table,
+// else four stages and one P buffer
+bool preferred(int B) { return mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB>::smem_bytes(B) <= optin_smem(); }
 
-template <int NS>
+template <int NS, int PB>
 cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    const int smem = mla::Layout<NS>::smem_bytes(a.B);
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = mla::Layout<NS, PB>::smem_bytes(a.B);
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<NS, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    mla_decode_kernel<NS><<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
+    mla_decode_kernel<NS, PB><<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
-template <int NS>
+template <int NS, int PB>
 int max_pairs_ns(int B) {
-    const int smem = mla::Layout<NS>::smem_bytes(B);
-    if (cudaFuncSetAttribute(mla_decode_kernel<NS>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    const int smem = mla::Layout<NS, PB>::smem_bytes(B);
+    if (cudaFuncSetAttribute(mla_decode_kernel<NS, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -712,15 +731,15 @@ int max_pairs_ns(int B) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<NS>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<NS, PB>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 }  // namespace
 
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    return five_stages(a.B) ? launch_ns<5>(maps, a, pairs, st) : launch_ns<4>(maps, a, pairs, st);
+    return preferred(a.B) ? launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(maps, a, pairs, st) : launch_ns<4, 1>(maps, a, pairs, st);
 }
 
-int max_pairs_mla(int B) { return five_stages(B) ? max_pairs_ns<5>(B) : max_pairs_ns<4>(B); }
+int max_pairs_mla(int B) { return preferred(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(B) : max_pairs_ns<4, 1>(B); }
 
 }  // namespace kvdec

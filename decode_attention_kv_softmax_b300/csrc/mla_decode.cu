@@ -40,7 +40,8 @@
 // running max grows by more than 2^8.
 // The split-KV schedule (schedule.cuh) gives each CTA pair an equal share of
 // all pages; sequences cut across pairs leave normalised partials, merged by
-// log-sum-exp ([ARG] §五.2) by the last piece to finish, per warp tile.
+// log-sum-exp ([ARG] §五.2) by the pair whose piece arrives last, once it has
+// finished its pages.
 #include "common.cuh"
 #include "kernels.h"
 #include "schedule.cuh"
@@ -74,7 +75,8 @@ struct Layout {
     static constexpr int kOffBars = kOffHand + kHandBytes;
     static constexpr int kBars = B_KV + 2 * NS;
     static constexpr int kOffMisc = kOffBars + ((kBars * 8 + 15) & ~15);   // [0] TMEM base, [1] abort word
-    static constexpr int kOffCum = kOffMisc + 16;
+    static constexpr int kOffPend = kOffMisc + 16;   // merges to do: [4 quadrants][count, b0, b1, -]
+    static constexpr int kOffCum = kOffPend + 64;
     static constexpr int smem_bytes(int B) { return kOffCum + (B + 1) * 4 + 1024; }
     static_assert(kOffRecv % 1024 == 0 && kOffP % 1024 == 0 && kOffQR % 1024 == 0, "alignment");
     static_assert(kThreads * 4 <= kRecvBytes, "scan scratch lives in the exchange buffer");
@@ -104,6 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     volatile int* abort_word = misc + 1;
     int* scratch = reinterpret_cast<int*>(smem + L::kOffRecv);   // free until the first exchange
     int* cum = reinterpret_cast<int*>(smem + L::kOffCum);
+    int* pend = reinterpret_cast<int*>(smem + L::kOffPend);
     const uint32_t sKV = smem_addr(smem + L::kOffKV);
     const uint32_t sQR = smem_addr(smem + L::kOffQR);
     const uint32_t sP = smem_addr(smem + L::kOffP);
@@ -126,6 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
             mbar_init(kv_empty(s), 1);
         }
         misc[1] = 0;
+        for (int q = 0; q < 4; ++q) pend[4 * q] = 0;
         fence_barrier_init();
     }
     if (warp == kSoftWarps) {
@@ -607,59 +611,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                                    ? 1
                                    : 0;
                     last = __shfl_sync(0xffffffffu, last, 0);
-                    if (last) {
-                        // merge this warp's 32 heads x 256 columns over every piece
-                        __threadfence();
-                        const int npc = S.num_pieces(cur.b, 0);
-                        int w0, kind0;
-                        S.first_piece(cur.b, 0, w0, kind0);
-                        float M = -INFINITY, den = 0.f;
-                        for (int s2 = 0; s2 < npc; ++s2) {
-                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                            M = fmaxf(M, __ldcg(plse + (size_t)sl * kHeads + row));
-                        }
-                        for (int s2 = 0; s2 < npc; ++s2) {
-                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                            const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
-                            den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
-                        }
-                        if (rank == 0 && a.lse) a.lse[orow] = den > 0.f ? M + __logf(den) : -INFINITY;
-                        const float invd = den > 0.f ? 1.f / den : 0.f;
-                        // 8 rows x 128 columns at a time, every row's load in flight together
-                        for (int r0 = 0; r0 < 64; r0 += 8) {
-                            const int rr = r0 & 31, ch = r0 >> 5;
-                            float4 acc[8];
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int s2 = 0; s2 < npc; ++s2) {
-                                const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                                const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
-                                const float wm = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * invd;
-                                const float4* src = reinterpret_cast<const float4*>(
-                                    a.part_o + ((size_t)sl * kHeads + qd * 32 + rr) * 512 + col0 + 128 * ch) + lane;
-                                float4 x[8];
-#pragma unroll
-                                for (int v = 0; v < 8; ++v) x[v] = __ldcg(src + (size_t)v * 128);
-#pragma unroll
-                                for (int v = 0; v < 8; ++v) {
-                                    const float wgt = __shfl_sync(0xffffffffu, wm, rr + v);
-                                    acc[v].x = fmaf(wgt, x[v].x, acc[v].x);
-                                    acc[v].y = fmaf(wgt, x[v].y, acc[v].y);
-                                    acc[v].z = fmaf(wgt, x[v].z, acc[v].z);
-                                    acc[v].w = fmaf(wgt, x[v].w, acc[v].w);
-                                }
-                            }
-#pragma unroll
-                            for (int v = 0; v < 8; ++v) {
-                                const size_t off =
-                                    ((size_t)cur.b * kHeads + qd * 32 + rr + v) * 512 + col0 + 128 * ch + 4 * lane;
-                                if (a.out_bf16)
-                                    *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
-                                        make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
-                                else
-                                    *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[v];
-                            }
-                        }
+                    // the last piece to arrive: the merge runs after the pages (at most
+                    // two per quadrant: only an item's first and last sequences are cut)
+                    if (last && lane == 0) {
+                        const int e = atomicAdd(pend + 4 * qd, 1);
+                        if (e < 2) pend[4 * qd + 1 + e] = cur.b;
                     }
                 }
             }
@@ -669,6 +625,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 if (cur.lt == 0) {
                     seg_start = j + k2;
                     ++seg_idx;
+                }
+            }
+        }
+
+        // ---- merges of the sequences whose last piece this CTA wrote, by
+        // log-sum-exp ([ARG] §五.2).  Both groups' warps of a quadrant take 128
+        // of the CTA's 256 columns each, 16 rows of loads in flight per warp
+        // (the registers of the page loop are free by now).
+        named_barrier(1, 32 * kSoftWarps);
+        __threadfence();
+        {
+            const float* plse = a.part_lse + (size_t)rank * (2 * npairs) * kHeads;
+            const int nm = min(pend[4 * qd], 2);
+            const int c0 = 256 * (int)rank + 128 * g;
+            for (int e = 0; e < nm; ++e) {
+                const int b = pend[4 * qd + 1 + e];
+                const int npc = S.num_pieces(b, 0);
+                int w0, kind0;
+                S.first_piece(b, 0, w0, kind0);
+                float M = -INFINITY, den = 0.f;
+                for (int s2 = 0; s2 < npc; ++s2) {
+                    const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
+                    M = fmaxf(M, __ldcg(plse + (size_t)sl * kHeads + row));
+                }
+                for (int s2 = 0; s2 < npc; ++s2) {
+                    const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
+                    const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
+                    den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                }
+                if (rank == 0 && g == 0 && a.lse) a.lse[(size_t)b * kHeads + row] = den > 0.f ? M + __logf(den) : -INFINITY;
+                const float invd = den > 0.f ? 1.f / den : 0.f;
+                for (int r0 = 0; r0 < 32; r0 += 16) {
+                    float4 acc[16];
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int s2 = 0; s2 < npc; ++s2) {
+                        const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
+                        const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
+                        const float wm = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * invd;
+                        const float4* src = reinterpret_cast<const float4*>(
+                            a.part_o + ((size_t)sl * kHeads + qd * 32 + r0) * 512 + c0) + lane;
+                        float4 x[16];
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) x[v] = __ldcg(src + (size_t)v * 128);
+#pragma unroll
+                        for (int v = 0; v < 16; ++v) {
+                            const float wgt = __shfl_sync(0xffffffffu, wm, r0 + v);
+                            acc[v].x = fmaf(wgt, x[v].x, acc[v].x);
+                            acc[v].y = fmaf(wgt, x[v].y, acc[v].y);
+                            acc[v].z = fmaf(wgt, x[v].z, acc[v].z);
+                            acc[v].w = fmaf(wgt, x[v].w, acc[v].w);
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v < 16; ++v) {
+                        const size_t off = ((size_t)b * kHeads + qd * 32 + r0 + v) * 512 + c0 + 4 * lane;
+                        if (a.out_bf16)
+                            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
+                                make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
+                        else
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[v];
+                    }
                 }
             }
         }

@@ -84,14 +84,15 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // box_cols x box_rows elements, given swizzle.
 kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
-                       CUtensorMapSwizzle swz) {
+                       CUtensorMapSwizzle swz,
+                       CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto enc = tensor_map_encoder();
     if (!enc) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {row_stride_bytes};
     const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+    CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
@@ -350,6 +351,15 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     kvdec::MlaMaps maps;
     if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
     if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+    // stores of O / l, 32 rows x 32 fp32 columns per box: partials, and out when it is fp32
+    if ((st = encode_2d(&maps.part, static_cast<uint8_t*>(p->workspace) + pl.off_o, 2 * (uint64_t)pl.pairs * 128, 512,
+                        2048, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
+        return st;
+    maps.outf = maps.part;
+    if (p->out_dtype == KVDEC_F32 &&
+        (st = encode_2d(&maps.outf, p->out, (uint64_t)p->batch * 128, 512, 2048, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
+        return st;
     kvdec::MlaArgs a;
     memset(&a, 0, sizeof(a));
     a.q_abs = static_cast<const __nv_bfloat16*>(p->q_absorbed);

@@ -235,6 +235,20 @@ KVDEC_DEVINL void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar
         : "memory");
 }
 
+// 2-D TMA store of a box from (swizzled) shared memory; completion tracked
+// by the issuing thread's bulk groups.
+KVDEC_DEVINL void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(c0), "r"(c1)
+                 : "memory");
+}
+KVDEC_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared memory of every committed bulk store has been read
+KVDEC_DEVINL void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// every committed bulk store has completed (its writes are done)
+KVDEC_DEVINL void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 KVDEC_DEVINL void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

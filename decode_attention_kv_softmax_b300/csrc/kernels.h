@@ -59,6 +59,8 @@ struct AppendArgs {
 struct MlaMaps {
     CUtensorMap c128;  // cache [pages*64, 576], box 64 x 64, 128-byte swizzle
     CUtensorMap c64;   // cache [pages*64, 576], box 32 x 64, 64-byte swizzle
+    CUtensorMap part;  // partial O [2*pairs*128, 512] fp32, box 32 x 32, 128-byte swizzle (stores)
+    CUtensorMap outf;  // out [B*128, 512] fp32, same box (stores; unused for bf16 out)
 };
 
 struct MlaArgs {

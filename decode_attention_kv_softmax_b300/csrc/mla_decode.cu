@@ -560,39 +560,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 const size_t orow = (size_t)cur.b * kHeads + row;
                 const int col0 = 256 * (int)rank;
                 // O / l goes out 32 columns at a time through this warp's quarter
-                // of the P buffer (32 rows x 128 B; chunk c of row r at chunk
-                // c ^ (r & 7)), so that every store writes whole lines: lane
-                // (r8, ch) writes 16-byte chunk ch of rows r8, r8 + 4, ...  PV(j)
-                // has read P(j); the next P waits for O_FREE.
+                // of the P buffer, 32 rows x 128 B with the 128-byte swizzle
+                // (chunk c of row r at chunk c ^ (r & 7)).  fp32 destinations
+                // (partials, fp32 out) take one TMA store per box; bf16 out is
+                // written by the lanes, whole 64-byte row pieces.  PV(j) has read
+                // P(j); the next P waits for O_FREE.
                 float* stg = reinterpret_cast<float*>(smem + L::kOffP + (PB == 2 ? g * kPBytes : 0) + qd * 4096);
+                const bool tma_out = !complete || !a.out_bf16;
+                const CUtensorMap* omap = complete ? &maps.outf : &maps.part;
+                const int drow = complete ? cur.b * kHeads + qd * 32 : slot * kHeads + qd * 32;
                 const int r8 = lane >> 3, ch = lane & 7;
-                const size_t drow0 = complete ? (size_t)cur.b * kHeads + qd * 32 : (size_t)slot * kHeads + qd * 32;
 #pragma unroll 1
                 for (int c0 = 0; c0 < 256; c0 += 32) {
                     float o[32];
                     tmem_ld16(trow + kTmemO + c0, *reinterpret_cast<float(*)[16]>(o));
                     tmem_ld16(trow + kTmemO + c0 + 16, *reinterpret_cast<float(*)[16]>(o + 16));
                     tmem_ld_wait();
+                    if (c0 > 0 && tma_out && lane == 0) bulk_wait_read_all();   // the last box left the buffer
+                    __syncwarp();
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<float4*>(stg + lane * 32 + ((c ^ (lane & 7)) << 2)) =
                             make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-                    __syncwarp();
+                    if (tma_out) {
+                        fence_proxy_async();
+                        __syncwarp();
+                        if (lane == 0) {
+                            tma_store_2d(omap, smem_addr(stg), col0 + c0, drow);
+                            bulk_commit();
+                        }
+                    } else {
+                        __syncwarp();
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        const int r = 4 * k + r8;
-                        const float4 v = *reinterpret_cast<const float4*>(stg + r * 32 + ((ch ^ (r & 7)) << 2));
-                        const size_t off = (drow0 + r) * 512 + col0 + c0 + 4 * ch;
-                        if (!complete)
-                            *reinterpret_cast<float4*>(a.part_o + off) = v;
-                        else if (a.out_bf16)
+                        for (int k = 0; k < 8; ++k) {
+                            const int r = 4 * k + r8;
+                            const float4 v = *reinterpret_cast<const float4*>(stg + r * 32 + ((ch ^ (r & 7)) << 2));
+                            const size_t off = ((size_t)drow + r) * 512 + col0 + c0 + 4 * ch;
                             *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
                                 make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-                        else
-                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = v;
+                        }
+                        __syncwarp();
                     }
-                    __syncwarp();
                 }
+                // the stores have read the buffer (the next P may go there) and
+                // written O (a merge may read it)
+                if (tma_out && lane == 0) {
+                    bulk_wait_all();
+                    asm volatile("fence.proxy.async;" ::: "memory");   // TMA writes -> generic readers
+                }
+                __syncwarp();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar(B_O_FREE));

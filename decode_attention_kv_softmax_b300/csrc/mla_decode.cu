@@ -382,7 +382,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 tc_fence_after();
                 load_q(cur.b);
             }
-            const int n_valid = min(kTileTokens, len - cur.lt * kTileTokens);
+            int n_valid = min(kTileTokens, len - cur.lt * kTileTokens);
+            if (n_valid < 1) {   // cannot happen with a consistent schedule; never index below the stage
+                report(a.err, KVDEC_DEVERR_SEQLEN);
+                n_valid = 0;
+            }
             const uint32_t u = (uint32_t)(j >> 1);   // use index of this group's buffers
 
             // ---- this CTA's partial S(j) -> registers

@@ -220,6 +220,7 @@ int64_t kvdec_params_size(int kind) {
         case 1: return (int64_t)sizeof(kvdec_mla_params);
         case 2: return (int64_t)sizeof(kvdec_append_params);
         case 3: return (int64_t)sizeof(kvdec_combine_params);
+        case 4: return (int64_t)sizeof(kvdec_mla_proj_params);
         default: return -1;
     }
 }
@@ -386,6 +387,34 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     cudaError_t e = kvdec::launch_mla(maps, a, pl.pairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
     return KVDEC_OK;
+}
+
+static kvdec_status mla_proj(const kvdec_mla_proj_params* p, void* stream, bool absorb) {
+    const char* name = absorb ? "kvdec_mla_absorb_q" : "kvdec_mla_project_out";
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "%s: params is NULL", name);
+    if (!p->x || !p->w || !p->y) return fail(KVDEC_ERR_INVALID_ARG, "%s: x, w and y must be non-NULL", name);
+    if (!aligned(p->x, 16) || !aligned(p->w, 16) || !aligned(p->y, 16))
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: x, w and y must be 16-byte aligned", name);
+    if (p->batch < 1 || p->batch > (1 << 20) || p->num_heads < 1 || p->num_heads > 65535)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: batch %d, num_heads %d", name, p->batch, p->num_heads);
+    if (p->out_dtype != KVDEC_F32 && p->out_dtype != KVDEC_BF16)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: out_dtype %d", name, p->out_dtype);
+    kvdec::MlaProjArgs a;
+    a.x = static_cast<const __nv_bfloat16*>(p->x);
+    a.w = static_cast<const __nv_bfloat16*>(p->w);
+    a.y = p->y;
+    a.batch = p->batch;
+    a.num_heads = p->num_heads;
+    a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    cudaError_t e = kvdec::launch_mla_proj(absorb, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return KVDEC_OK;
+}
+
+kvdec_status kvdec_mla_absorb_q(const kvdec_mla_proj_params* p, void* stream) { return mla_proj(p, stream, true); }
+
+kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream) {
+    return mla_proj(p, stream, false);
 }
 
 kvdec_status kvdec_combine_splits(const kvdec_combine_params* p, void* stream) {

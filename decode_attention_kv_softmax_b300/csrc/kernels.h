@@ -82,7 +82,15 @@ struct MlaArgs {
     uint64_t timeout_ns;
 };
 
+struct MlaProjArgs {
+    const __nv_bfloat16* x;   // absorb: q_nope [B, H, 128]; project: latent [B, H, 512]
+    const __nv_bfloat16* w;   // [H, 128, 512]
+    void* y;                  // absorb: [B, H, 512]; project: [B, H, 128]
+    int batch, num_heads, out_bf16;
+};
+
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st);
+cudaError_t launch_mla_proj(bool absorb, const MlaProjArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
 
 cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -61,11 +61,16 @@ class CombineParams(ctypes.Structure):
                 ("lse", c_void_p)]
 
 
+class MlaProjParams(ctypes.Structure):
+    _fields_ = [("x", c_void_p), ("w", c_void_p), ("y", c_void_p), ("batch", c_int32),
+                ("num_heads", c_int32), ("out_dtype", c_int32), ("reserved", c_int32)]
+
+
 EXPORTS = ["kvdec_abi_version", "kvdec_params_size", "kvdec_status_string",
            "kvdec_last_error", "kvdec_gqa_workspace_bytes", "kvdec_gqa_decode",
            "kvdec_mla_workspace_bytes", "kvdec_mla_decode_absorbed", "kvdec_append_rope",
            "kvdec_combine_splits", "kvdec_selftest_wait_timeout",
-           "kvdec_gqa_decode_noalloc"]
+           "kvdec_gqa_decode_noalloc", "kvdec_mla_absorb_q", "kvdec_mla_project_out"]
 
 _lib = None
 _lock = threading.Lock()
@@ -95,7 +100,9 @@ def load(path: str = LIB_PATH):
         for name, st in [("kvdec_gqa_decode", GqaParams), ("kvdec_gqa_decode_noalloc", GqaParams),
                          ("kvdec_mla_decode_absorbed", MlaParams),
                          ("kvdec_append_rope", AppendParams),
-                         ("kvdec_combine_splits", CombineParams)]:
+                         ("kvdec_combine_splits", CombineParams),
+                         ("kvdec_mla_absorb_q", MlaProjParams),
+                         ("kvdec_mla_project_out", MlaProjParams)]:
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(st), c_void_p]
@@ -103,7 +110,7 @@ def load(path: str = LIB_PATH):
         lib.kvdec_selftest_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
         if lib.kvdec_abi_version() != 1:
             raise RuntimeError("libkvdec ABI version mismatch")
-        for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams]):
+        for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams, MlaProjParams]):
             if lib.kvdec_params_size(kind) != ctypes.sizeof(st):
                 raise RuntimeError(f"params struct {st.__name__} layout mismatch")
         _lib = lib
@@ -395,6 +402,40 @@ def combine_splits(partial_o, partial_lse, split_counts=None, out_dtype=torch.fl
     p.out, p.lse = _ptr(out), _ptr(lse)
     _check(lib.kvdec_combine_splits(ctypes.byref(p), _stream(stream)), "kvdec_combine_splits")
     return out, lse
+
+
+def _mla_proj(fn, name, x, w, width, out_dtype, out, stream):
+    lib = load()
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev)
+    _need(w, "w", torch.bfloat16, dev)
+    B, H, _ = x.shape
+    if tuple(w.shape) != (H, 128, 512):
+        raise ValueError(f"{name}: w must be [{H}, 128, 512], got {tuple(w.shape)}")
+    if out is None:
+        out = torch.empty((B, H, width), dtype=out_dtype, device=dev)
+    p = MlaProjParams()
+    p.x, p.w, p.y = _ptr(x), _ptr(w), _ptr(out)
+    p.batch, p.num_heads = B, H
+    p.out_dtype = _dtype_code(out.dtype)
+    _check(getattr(lib, fn)(ctypes.byref(p), _stream(stream)), fn)
+    return out
+
+
+def mla_absorb_q(q_nope, W_UK, out_dtype=torch.bfloat16, out=None, stream=None):
+    """q_absorbed[b,h] = W_UK[h]^T q_nope[b,h]: q_nope [B,H,128] bf16, W_UK
+    [H,128,512] bf16 -> [B,H,512] (bf16 by default: the decode's input)."""
+    if q_nope.shape[-1] != 128:
+        raise ValueError("mla_absorb_q: q_nope must be [B, H, 128]")
+    return _mla_proj("kvdec_mla_absorb_q", "mla_absorb_q", q_nope, W_UK, 512, out_dtype, out, stream)
+
+
+def mla_project_out(latent, W_UV, out_dtype=torch.float32, out=None, stream=None):
+    """out[b,h] = W_UV[h] latent[b,h]: latent [B,H,512] bf16, W_UV [H,128,512]
+    bf16 -> [B,H,128]."""
+    if latent.shape[-1] != 512:
+        raise ValueError("mla_project_out: latent must be [B, H, 512]")
+    return _mla_proj("kvdec_mla_project_out", "mla_project_out", latent, W_UV, 128, out_dtype, out, stream)
 
 
 def selftest_wait_timeout(timeout_ns: int, error_flag, stream=None):

@@ -252,6 +252,39 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream);
 /* ------------------------------------------------------------------------ */
 /* Split combine                                                             */
 /* ------------------------------------------------------------------------ */
+/* ---------------------------------------------------------------- MLA projections
+ * The two absorbed projections around kvdec_mla_decode_absorbed ([ARG]
+ * "attention-variants-and-kv-cache" §四.5; [MLA] "multi-head-latent-
+ * attention" §4): for every sequence b and head h,
+ *   kvdec_mla_absorb_q:    q_absorbed[b,h,:] = W_UK[h]^T q_nope[b,h,:]   (128 -> 512)
+ *   kvdec_mla_project_out: out[b,h,:]        = W_UV[h]   latent[b,h,:]   (512 -> 128)
+ * with W_UK, W_UV [num_heads, 128, 512] bf16 (row v or d of head h holds the
+ * 512 latent weights).  Together with the decode they give one MLA attention
+ * layer in value space; the pages carry no counterpart kernel, only the
+ * algebra.
+ *
+ * Layouts (row-major, bf16 inputs, fp32 accumulation):
+ *   absorb:  x = q_nope bf16 [batch, num_heads, 128], y [batch, num_heads, 512]
+ *   project: x = latent bf16 [batch, num_heads, 512], y [batch, num_heads, 128]
+ *   y is F32 or BF16 (out_dtype).
+ * Ownership: the caller owns every buffer; nothing is allocated.
+ * Errors: KVDEC_ERR_INVALID_ARG for NULL or misaligned (16 B) pointers, a
+ * batch or head count below 1 (batch above 2^20), or another out_dtype; the
+ * call is asynchronous on `stream`.
+ */
+typedef struct kvdec_mla_proj_params {
+    const void* x;
+    const void* w;
+    void* y;
+    int32_t batch;
+    int32_t num_heads;
+    int32_t out_dtype;
+    int32_t reserved;
+} kvdec_mla_proj_params;
+
+kvdec_status kvdec_mla_absorb_q(const kvdec_mla_proj_params* p, void* stream);
+kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream);
+
 /*
  * Merges normalised split partials of rows = batch * num_heads rows
  * ([ARG] §五.2, last paragraph: softmax each piece locally, then merge the

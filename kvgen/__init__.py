@@ -184,6 +184,18 @@ def mla_case(B, n_h=128, *, seqlens=None, lo=None, hi=None, seed=SEED_BASE,
     return MlaCase(q_abs, q_rope, cache, sl, bt, scale, {"num_pages": num_pages})
 
 
+def mla_proj_case(B, n_h=128, *, seed=SEED_BASE, device="cpu"):
+    """Inputs of the two MLA absorption projections: q_nope [B, n_h, 128],
+    W_UK and W_UV [n_h, 128, 512], all bf16 ~ N(0, 1) scaled so that every
+    output element has unit variance (W_UK by 1/sqrt(128): 128 terms;
+    W_UV by 1/sqrt(512): 512 terms)."""
+    g = _gen(seed, device)
+    q_nope = _randn_bf16((B, n_h, 128), g, device)
+    W_UK = _randn_bf16((n_h, 128, D_C), g, device, std=1.0 / math.sqrt(128))
+    W_UV = _randn_bf16((n_h, 128, D_C), g, device, std=1.0 / math.sqrt(D_C))
+    return q_nope, W_UK, W_UV
+
+
 # ----------------------------------------------------------------------------
 # the five named workloads
 # ----------------------------------------------------------------------------

@@ -12,7 +12,7 @@ citations.  Parity pins (tests that tie each function to something other than
 itself) live in ``tests/test_oracle_pins.py``.
 """
 from .attention import (  # noqa: F401
-    attend, gqa_decode, mla_decode_absorbed, mla_decode_nonabsorbed,
+    attend, gqa_decode, mla_decode_absorbed, mla_absorb_q, mla_project_out, mla_decode_nonabsorbed,
     combine_splits, split_partials, rope_rotate, rope_matrix,
     append_rope_mla, append_rope_gqa, bf16_to_f64, f64_to_bf16_bits,
     bf16_bits_to_f64, gather_tokens,

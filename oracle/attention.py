@@ -207,6 +207,31 @@ def mla_decode_nonabsorbed(q_nope, q_rope, cache, block_table, seqlens,
 # ----------------------------------------------------------------------------
 # flash-decoding split and merge ([ARG] §五.2, last paragraph: split the KV
 # along the sequence, softmax each piece locally, then merge the normalisers)
+def mla_absorb_q(q_nope, W_UK):
+    """Query-side absorption ([ARG] "attention-variants-and-kv-cache" §四.5;
+    [MLA] "multi-head-latent-attention" §4): q~_{b,h} = W_UK,h^T q^C_{b,h},
+    the 128-wide per-head no-rope query taken into the 512-wide latent space,
+    so that q~_{b,h} . c = q^C_{b,h} . (W_UK,h c).  q_nope [B, n_h, d_h],
+    W_UK [n_h, d_h, 512] -> [B, n_h, 512]."""
+    B, n_h, d_h = q_nope.shape
+    out = np.zeros((B, n_h, W_UK.shape[2]))
+    for h in range(n_h):
+        out[:, h, :] = q_nope[:, h, :] @ W_UK[h]
+    return out
+
+
+def mla_project_out(lat, W_UV):
+    """Value-side absorption ([ARG] §四.5; [MLA] §4): the latent output
+    o~_{b,h} = sum_j p_j c_j taken to head h's value space,
+    o_{b,h} = W_UV,h o~_{b,h} = sum_j p_j (W_UV,h c_j).  lat [B, n_h, 512],
+    W_UV [n_h, d_v, 512] -> [B, n_h, d_v]."""
+    B, n_h, _ = lat.shape
+    out = np.zeros((B, n_h, W_UV.shape[1]))
+    for h in range(n_h):
+        out[:, h, :] = lat[:, h, :] @ W_UV[h].T
+    return out
+
+
 # ----------------------------------------------------------------------------
 
 

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
 def test_struct_layouts(lib):
     assert lib.kvdec_abi_version() == 1
     for kind, st in enumerate([kvdec.GqaParams, kvdec.MlaParams, kvdec.AppendParams,
-                               kvdec.CombineParams]):
+                               kvdec.CombineParams, kvdec.MlaProjParams]):
         assert lib.kvdec_params_size(kind) == ctypes.sizeof(st)
     assert lib.kvdec_params_size(99) == -1
 
@@ -68,3 +68,21 @@ def test_host_argument_checks(lib):
     m = kvdec.MlaParams()
     assert lib.kvdec_mla_decode_absorbed(ctypes.byref(m), None) != 0
     assert lib.kvdec_selftest_wait_timeout(1000, None, None) == 1
+
+
+def test_projection_argument_checks(lib):
+    """The MLA projections reject bad arguments before any launch."""
+    assert lib.kvdec_mla_absorb_q(None, None) == 1
+    p = kvdec.MlaProjParams()
+    assert lib.kvdec_mla_project_out(ctypes.byref(p), None) == 1
+    assert "non-NULL" in lib.kvdec_last_error().decode()
+    p.x, p.w, p.y = 256, 512, 1024          # aligned, never dereferenced on the host
+    p.batch, p.num_heads, p.out_dtype = 0, 128, kvdec.F32
+    assert lib.kvdec_mla_absorb_q(ctypes.byref(p), None) == 1
+    assert "batch" in lib.kvdec_last_error().decode()
+    p.batch, p.out_dtype = 4, 7
+    assert lib.kvdec_mla_project_out(ctypes.byref(p), None) == 1
+    assert "out_dtype" in lib.kvdec_last_error().decode()
+    p.out_dtype, p.x = kvdec.F32, 257
+    assert lib.kvdec_mla_absorb_q(ctypes.byref(p), None) == 1
+    assert "aligned" in lib.kvdec_last_error().decode()

@@ -214,12 +214,14 @@ def test_mla_absorbed_equals_nonabsorbed():
     W_UK = RNG.normal(size=(n_h, 128, 512)) / math.sqrt(512)
     W_UV = RNG.normal(size=(n_h, 128, 512)) / math.sqrt(512)
     q_nope = RNG.normal(size=(B, n_h, 128))
-    q_abs = np.einsum("bhd,hdc->bhc", q_nope, W_UK)
+    q_abs = oracle.mla_absorb_q(q_nope, W_UK)
     lat, lse_a = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl)
-    o_abs = np.einsum("hvc,bhc->bhv", W_UV, lat)
+    o_abs = oracle.mla_project_out(lat, W_UV)
     o_ref, lse_n = oracle.mla_decode_nonabsorbed(q_nope, q_rope, cache, bt, sl, W_UK, W_UV)
     np.testing.assert_allclose(o_abs, o_ref, atol=1e-11)
     np.testing.assert_allclose(lse_a, lse_n, atol=1e-11)
+    # a transposed head weight (a plausible slip) does not reach the same output
+    assert not np.allclose(oracle.mla_project_out(lat, W_UV[:, :, ::-1]), o_ref, atol=1e-3)
     # 1/sqrt(576) is a different (wrong) reading and shows up
     lat2, _ = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl, scale=1 / 24.0)
     assert not np.allclose(lat2, lat, atol=1e-6)

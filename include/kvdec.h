@@ -249,10 +249,11 @@ typedef struct kvdec_append_params {
 
 kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream);
 
+
 /* ------------------------------------------------------------------------ */
-/* Split combine                                                             */
+/* MLA absorption projections                                                */
 /* ------------------------------------------------------------------------ */
-/* ---------------------------------------------------------------- MLA projections
+/*
  * The two absorbed projections around kvdec_mla_decode_absorbed ([ARG]
  * "attention-variants-and-kv-cache" §四.5; [MLA] "multi-head-latent-
  * attention" §4): for every sequence b and head h,
@@ -285,6 +286,9 @@ typedef struct kvdec_mla_proj_params {
 kvdec_status kvdec_mla_absorb_q(const kvdec_mla_proj_params* p, void* stream);
 kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream);
 
+/* ------------------------------------------------------------------------ */
+/* Split combine                                                             */
+/* ------------------------------------------------------------------------ */
 /*
  * Merges normalised split partials of rows = batch * num_heads rows
  * ([ARG] §五.2, last paragraph: softmax each piece locally, then merge the

@@ -58,6 +58,10 @@ class GqaCase:
     scale: float
     cap: int                          # tokens addressable per sequence
     meta: dict = field(default_factory=dict)
+    # E4M3 caches: k, v hold uint8 codes and these the per-KV-head fp32 scales
+    k_scale: torch.Tensor | None = None
+    v_scale: torch.Tensor | None = None
+    window: int = 0                   # > 0: ring cache of the last `window` tokens
 
     @property
     def B(self):
@@ -142,10 +146,15 @@ def shuffled_block_table(seqlens: torch.Tensor, g, device, spare_pages: int = 0,
 
 def gqa_case(B, h, n_kv, d, *, seqlens=None, lo=None, hi=None, cap=None,
              paged=False, seed=SEED_BASE, device="cpu", q=None,
-             spare_pages=0, scale=None) -> GqaCase:
+             spare_pages=0, scale=None, kv_dtype="bf16", window=0) -> GqaCase:
     """Build a GQA decode problem.  Either pass explicit ``seqlens`` (list or
-    tensor) or a range [lo, hi].  ``cap`` defaults to max(seqlen) rounded up
-    to PAGE for contiguous caches."""
+    tensor) or a range [lo, hi].  ``cap`` defaults to the longest cached
+    length rounded up to PAGE for contiguous caches.
+
+    ``window`` > 0 makes a ring cache of ``window`` slots: seqlens count every
+    token of the sequence (and may exceed the capacity) while only
+    min(seqlen, window) slots hold data.  ``kv_dtype="fp8"`` turns K and V
+    into E4M3 codes (see fp8_codes)."""
     g = _gen(seed, device)
     if seqlens is None:
         sl = draw_seqlens(B, lo, hi, g, device)
@@ -155,18 +164,43 @@ def gqa_case(B, h, n_kv, d, *, seqlens=None, lo=None, hi=None, cap=None,
         q = _randn_bf16((B, h, d), g, device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
+    held = sl.clamp(max=window) if window > 0 else sl      # slots holding data
     if not paged:
         if cap is None:
-            mx = int(sl.max().item()) if B > 0 else 0
+            mx = int(held.max().item()) if B > 0 else 0
             cap = max(PAGE, (mx + PAGE - 1) // PAGE * PAGE)
         k = _randn_bf16((B, n_kv, cap, d), g, device)
         v = _randn_bf16((B, n_kv, cap, d), g, device)
-        return GqaCase(q, k, v, sl, None, scale, cap)
-    bt, num_pages = shuffled_block_table(sl, g, device, spare_pages)
-    k = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
-    v = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
-    cap = bt.shape[1] * PAGE
-    return GqaCase(q, k, v, sl, bt, scale, cap, {"num_pages": num_pages})
+        case = GqaCase(q, k, v, sl, None, scale, cap, window=window)
+    else:
+        bt, num_pages = shuffled_block_table(held, g, device, spare_pages)
+        k = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
+        v = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
+        cap = bt.shape[1] * PAGE
+        case = GqaCase(q, k, v, sl, bt, scale, cap, {"num_pages": num_pages},
+                       window=window)
+    if kv_dtype == "fp8":
+        case.k, case.k_scale = fp8_codes(case.k, g, device)
+        case.v, case.v_scale = fp8_codes(case.v, g, device)
+    elif kv_dtype != "bf16":
+        raise ValueError(kv_dtype)
+    return case
+
+
+def fp8_codes(x: torch.Tensor, g, device):
+    """Stand-in for a quantised E4M3 cache with one scale per KV head (axis
+    1): each head's values are the drawn N(0,1) values times a per-head
+    spread sigma_h ~ U[0.25, 4] (so that a scale taken from the wrong head is
+    visible), cast by torch to float8_e4m3fn with scale_h = max|x_h| / 448.
+    Returns (uint8 codes of x's shape, fp32 scales [n_kv])."""
+    n_kv = x.shape[1]
+    sigma = torch.empty(n_kv, device=device).uniform_(0.25, 4.0, generator=g)
+    xs = x.float() * sigma.view(1, -1, 1, 1)
+    amax = xs.abs().amax(dim=(0, 2, 3)).clamp(min=1e-6)
+    scale = (amax / 448.0).to(torch.float32)
+    codes = (xs / scale.view(1, -1, 1, 1)).clamp(-448.0, 448.0)
+    codes = codes.to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
 
 
 def mla_case(B, n_h=128, *, seqlens=None, lo=None, hi=None, seed=SEED_BASE,

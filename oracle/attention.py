@@ -78,6 +78,69 @@ def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
 
 
 # ----------------------------------------------------------------------------
+# E4M3, the 8-bit float of an FP8 KV cache ([ARG] §六.3: FP8 (E4M3) halves the
+# bytes per element, with one scale per head or per token).  The format is the
+# E4M3 of "FP8 Formats for Deep Learning" (Micikevicius et al., 2022): 1 sign
+# bit, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 holds
+# the subnormals (m/8) * 2^-6; S.1111.111 is NaN; there is no infinity, so
+# the largest finite magnitude is 1.75 * 2^8 = 448.
+# ----------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3_bits_to_f64(codes) -> np.ndarray:
+    """Exact value of each E4M3 code (uint8 array)."""
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    mag = np.where((c & 0x7F) == 0x7F, np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+# magnitudes of codes 0x00..0x7E, strictly increasing with the code
+_E4M3_MAGS = e4m3_bits_to_f64(np.arange(0x7F))
+
+
+def f64_to_e4m3_bits(x) -> np.ndarray:
+    """Nearest E4M3 code to each value, ties to the even code (mantissa LSB
+    0); magnitudes above 448 saturate to 448; NaN gives 0x7F; the sign bit is
+    the input's (so a negative value that rounds to zero gives 0x80)."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.minimum(np.abs(np.nan_to_num(x)), E4M3_MAX)
+    hi = np.searchsorted(_E4M3_MAGS, a, side="left")      # first magnitude >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a - _E4M3_MAGS[lo]
+    d_hi = _E4M3_MAGS[hi] - a
+    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(take_hi, hi, lo)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    code = np.where(np.isnan(x), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def dequant_e4m3(codes, scale, head_axis: int = 1) -> np.ndarray:
+    """Cache values of an FP8 cache with one scale per KV head ([ARG] §六.3):
+    value = E4M3(code) * scale[head], the head on ``head_axis`` (1 for both
+    the contiguous [B, n_kv, cap, d] and the paged [pages, n_kv, PAGE, d]
+    layouts)."""
+    v = e4m3_bits_to_f64(codes)
+    shape = [1] * v.ndim
+    shape[head_axis] = -1
+    return v * np.asarray(scale, dtype=np.float64).reshape(shape)
+
+
+def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seqlens, scale=None,
+                   block_table=None, window=0):
+    """GQA decode over an E4M3 K/V cache with per-KV-head scales: the plain
+    decode of the dequantised cache ([ARG] §六.3: quantisation changes only
+    the bytes per element, not the attention)."""
+    return gqa_decode(q, dequant_e4m3(k_codes, k_scale), dequant_e4m3(v_codes, v_scale),
+                      seqlens, scale, block_table, window)
+
+
+# ----------------------------------------------------------------------------
 # softmax attention of one query block over one key/value sequence
 # ----------------------------------------------------------------------------
 
@@ -103,27 +166,48 @@ def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, scale: float):
     return out, lse
 
 
-def gather_tokens(cache, b: int, L: int, block_table=None, head=None):
-    """Rows 0..L-1 of sequence b.  Contiguous caches are [B, heads, cap, d]
-    (head given) or [B, cap, d]; paged caches are [pages, heads, PAGE, d] or
-    [pages, PAGE, d] with token j at (block_table[b, j // PAGE], j % PAGE)
-    ([ARG] §六.1: the kernel looks up logical -> physical block)."""
-    j = np.arange(L)
+def gather_slots(cache, b: int, slots, block_table=None, head=None):
+    """Cache rows ``slots`` of sequence b.  Contiguous caches are
+    [B, heads, cap, d] (head given) or [B, cap, d]; paged caches are
+    [pages, heads, PAGE, d] or [pages, PAGE, d] with slot j at
+    (block_table[b, j // PAGE], j % PAGE) ([ARG] §六.1: the kernel looks up
+    logical -> physical block)."""
+    j = np.asarray(slots, dtype=np.int64)
     if block_table is None:
-        return cache[b, head, :L] if head is not None else cache[b, :L]
+        return cache[b, head, j] if head is not None else cache[b, j]
     pages = np.asarray(block_table)[b, j // PAGE]
     if head is not None:
         return cache[pages, head, j % PAGE]
     return cache[pages, j % PAGE]
 
 
-def gqa_decode(q, k, v, seqlens, scale=None, block_table=None):
+def gather_tokens(cache, b: int, L: int, block_table=None, head=None):
+    """Rows 0..L-1 of sequence b (see gather_slots)."""
+    return gather_slots(cache, b, np.arange(L), block_table, head)
+
+
+def window_slots(n: int, window: int) -> np.ndarray:
+    """Cache slots a decode step reads for a sequence of n tokens.
+
+    window = 0: every position 0..n-1, slot = position.  window = w > 0
+    (sliding-window attention, [ARG] §五.3 and its mask figure): the query at
+    position t = n-1 sees the w positions t-w+1 .. t (the figure marks w
+    cells per row; the text's "[t - w, t]" would be w+1 -- reading: w), and
+    the cache keeps only those, so position p lives in ring slot p mod w."""
+    if window <= 0:
+        return np.arange(n)
+    pos = np.arange(max(0, n - window), n)
+    return pos % window
+
+
+def gqa_decode(q, k, v, seqlens, scale=None, block_table=None, window=0):
     """MHA / GQA / MQA decode ([ARG] §三.2; [CH7] §7.3; [KVC-LLM] §四).
 
     q [B, h, d]; k, v contiguous [B, n_kv, cap, d] or paged
     [pages, n_kv, PAGE, d] with block_table [B, max_blocks].  Query head hh
-    reads KV head hh // g, g = h / n_kv.  Returns out [B, h, d], lse [B, h]
-    (natural log)."""
+    reads KV head hh // g, g = h / n_kv.  ``window`` > 0 reads a ring cache
+    of the last ``window`` positions (window_slots).  Returns out [B, h, d],
+    lse [B, h] (natural log)."""
     B, h, d = q.shape
     n_kv = k.shape[1]
     assert h % n_kv == 0
@@ -133,11 +217,11 @@ def gqa_decode(q, k, v, seqlens, scale=None, block_table=None):
     out = np.zeros((B, h, d))
     lse = np.zeros((B, h))
     for b in range(B):
-        L = int(seqlens[b])
+        slots = window_slots(int(seqlens[b]), window)
         for hh in range(h):
             kv = hh // g
-            K = gather_tokens(k, b, L, block_table, kv)
-            V = gather_tokens(v, b, L, block_table, kv)
+            K = gather_slots(k, b, slots, block_table, kv)
+            V = gather_slots(v, b, slots, block_table, kv)
             o, l = attend(q[b, hh:hh + 1], K, V, scale)
             out[b, hh] = o[0]
             lse[b, hh] = l[0]
@@ -322,21 +406,41 @@ def append_rope_mla(cache_bits, block_table, seqlens, c_kv_bits, kr_bits,
 
 
 def append_rope_gqa(k_bits, v_bits, seqlens, k_new_bits, v_new_bits,
-                    block_table=None, theta=10000.0):
-    """GQA cache append: K[.., pos, :] = RoPE_pos(k_new) over the whole head
-    dim, V[.., pos, :] = v_new.  Contiguous [B, n_kv, cap, d] or paged
-    [pages, n_kv, PAGE, d] layouts; bf16 bit patterns in and out."""
+                    block_table=None, theta=10000.0, window=0, k_scale=None,
+                    v_scale=None):
+    """GQA cache append: K[.., slot, :] = RoPE_pos(k_new) over the whole head
+    dim, V[.., slot, :] = v_new, pos = seqlens[b].  slot = pos, or pos mod
+    window for a sliding-window ring cache ([ARG] §五.3: the cache keeps the
+    last window tokens).  Contiguous [B, n_kv, cap, d] or paged
+    [pages, n_kv, PAGE, d] layouts.
+
+    bf16 cache (k_scale None): bf16 bit patterns in and out.  E4M3 cache
+    (k_scale, v_scale fp32 [n_kv], [ARG] §六.3): K code = E4M3(RoPE(k) /
+    k_scale) from the binary64 rotation; V code = E4M3(v / v_scale) taken
+    from the binary32 quotient -- the quantised code is decided in the
+    precision the kernel divides in, so V codes are exact while K codes carry
+    the rotation's rounding (within one code)."""
     K = np.array(k_bits, copy=True)
     V = np.array(v_bits, copy=True)
     B, n_kv, d = k_new_bits.shape
+    fp8 = k_scale is not None
     for b in range(B):
         pos = int(seqlens[b])
-        rot = f64_to_bf16_bits(rope_rotate(bf16_bits_to_f64(k_new_bits[b]), pos, theta))
-        if block_table is None:
-            K[b, :, pos] = rot
-            V[b, :, pos] = v_new_bits[b]
+        slot = pos % window if window > 0 else pos
+        rot = rope_rotate(bf16_bits_to_f64(k_new_bits[b]), pos, theta)
+        if fp8:
+            kq = f64_to_e4m3_bits(rot / np.asarray(k_scale, np.float64)[:, None])
+            vq32 = (bf16_bits_to_f64(v_new_bits[b]).astype(np.float32)
+                    / np.asarray(v_scale, np.float32)[:, None])
+            vq = f64_to_e4m3_bits(vq32.astype(np.float64))
         else:
-            page = int(block_table[b, pos // PAGE])
-            K[page, :, pos % PAGE] = rot
-            V[page, :, pos % PAGE] = v_new_bits[b]
+            kq = f64_to_bf16_bits(rot)
+            vq = v_new_bits[b]
+        if block_table is None:
+            K[b, :, slot] = kq
+            V[b, :, slot] = vq
+        else:
+            page = int(block_table[b, slot // PAGE])
+            K[page, :, slot % PAGE] = kq
+            V[page, :, slot % PAGE] = vq
     return K, V

@@ -220,7 +220,7 @@ def test_mla_absorbed_equals_nonabsorbed():
     o_ref, lse_n = oracle.mla_decode_nonabsorbed(q_nope, q_rope, cache, bt, sl, W_UK, W_UV)
     np.testing.assert_allclose(o_abs, o_ref, atol=1e-11)
     np.testing.assert_allclose(lse_a, lse_n, atol=1e-11)
-    # a transposed head weight (a plausible slip) does not reach the same output
+    # W_UV with its latent axis reversed (a plausible slip) does not reach the same output
     assert not np.allclose(oracle.mla_project_out(lat, W_UV[:, :, ::-1]), o_ref, atol=1e-3)
     # 1/sqrt(576) is a different (wrong) reading and shows up
     lat2, _ = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl, scale=1 / 24.0)
@@ -352,6 +352,195 @@ def test_append_gqa_contiguous_and_paged():
     Kp2, Vp2 = oracle.append_rope_gqa(Kp, Vp, np.array([70, 3]), kn, vn, block_table=bt)
     np.testing.assert_array_equal(Vp2[0, :, 6], vn[0])
     np.testing.assert_array_equal(Vp2[2, :, 3], vn[1])
+
+
+# ---------------------------------------------------------------- E4M3 (FP8 KV cache)
+
+def test_e4m3_decode_golden():
+    """Code values written out from the format definition."""
+    for key, (val,) in read_golden("e4m3_codes.txt").items():
+        code = int(key[4:])
+        got = oracle.e4m3_bits_to_f64(np.array([code], np.uint8))[0]
+        assert got == val and np.signbit(got) == np.signbit(val), (code, got, val)
+    assert np.isnan(oracle.e4m3_bits_to_f64(np.array([0x7F, 0xFF], np.uint8))).all()
+
+
+def test_e4m3_decode_matches_library_cast():
+    """All 256 codes against torch's float8_e4m3fn widening."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_bits_to_f64(codes)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+
+
+def test_e4m3_encode_matches_library_cast():
+    """Nearest-even rounding against torch's float32 -> float8_e4m3fn cast on
+    values across the whole finite range, including every midpoint between
+    neighbouring codes (the ties)."""
+    mags = oracle.e4m3_bits_to_f64(np.arange(0x7F))
+    mids = (mags[:-1] + mags[1:]) / 2
+    rnd = np.exp2(RNG.uniform(-12, np.log2(448.0), 20000))
+    x = np.concatenate([mags, mids, rnd, np.nextafter(mids, 0), np.nextafter(mids, 1e9)])
+    x = np.concatenate([x, -x]).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle.f64_to_e4m3_bits(x.astype(np.float64))
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_e4m3_encode_ties_saturation_roundtrip():
+    enc = oracle.f64_to_e4m3_bits
+    # ties go to the even code: 1.0625 between 1 (0x38) and 1.125 (0x39)
+    assert enc([1.0625])[0] == 0x38 and enc([1.1875])[0] == 0x3A
+    # subnormal ties: 2^-10 between 0 and 2^-9; 3 * 2^-10 between codes 1 and 2
+    assert enc([2.0 ** -10])[0] == 0x00 and enc([3 * 2.0 ** -10])[0] == 0x02
+    # saturation to the largest finite value, sign kept
+    assert enc([1e6])[0] == 0x7E and enc([-500.0])[0] == 0xFE and enc([464.0])[0] == 0x7E
+    assert enc([np.nan])[0] == 0x7F and enc([-0.0])[0] == 0x80
+    finite = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    np.testing.assert_array_equal(enc(oracle.e4m3_bits_to_f64(finite)), finite)
+
+
+def test_dequant_scales_the_kv_head_axis():
+    codes = np.full((2, 3, 5, 4), 0x38, np.uint8)          # every value 1.0
+    sc = np.array([0.5, 2.0, 8.0])
+    v = oracle.dequant_e4m3(codes, sc)
+    for hh in range(3):
+        assert np.all(v[:, hh] == sc[hh])
+
+
+def test_fp8_decode_equals_decode_of_dequantised_bf16():
+    """With power-of-two scales every dequantised value is a bf16 number, so
+    the FP8 decode must equal the bf16 decode of the same values; a scale
+    taken from the wrong head, or K's scale used for V, must not."""
+    c = kvgen.gqa_case(2, 8, 2, 16, seqlens=[9, 70], seed=3)
+    kc = RNG.integers(0, 256, c.k.shape).astype(np.uint8)
+    vc = RNG.integers(0, 256, c.v.shape).astype(np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x3C                      # no NaN codes
+    vc[(vc & 0x7F) == 0x7F] = 0x3C
+    kc = kc & 0xBF                                       # exponent field <= 7: |value| < 2
+    vc = vc & 0xBF
+    ks = np.array([2.0 ** -3, 2.0 ** 1])
+    vs = np.array([2.0 ** 2, 2.0 ** -1])
+    q = oracle.bf16_to_f64(c.q)
+    out, lse = oracle.gqa_decode_fp8(q, kc, vc, ks, vs, c.seqlens.numpy())
+    kf = oracle.e4m3_bits_to_f64(kc) * ks[None, :, None, None]
+    vf = oracle.e4m3_bits_to_f64(vc) * vs[None, :, None, None]
+    assert np.array_equal(oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(kf)), kf)
+    out2, lse2 = oracle.gqa_decode(q, kf, vf, c.seqlens.numpy())
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+    bad, _ = oracle.gqa_decode_fp8(q, kc, vc, ks[::-1], vs, c.seqlens.numpy())
+    assert not np.allclose(bad, out, atol=1e-3)
+    bad, _ = oracle.gqa_decode_fp8(q, kc, vc, ks, ks, c.seqlens.numpy())
+    assert not np.allclose(bad, out, atol=1e-3)
+
+
+def test_fp8_append_codes():
+    """FP8 append: K codes are the nearest codes to RoPE(k) / k_scale (the
+    quantisation error bound: half a code step); V codes equal the library
+    cast of the binary32 quotient v / v_scale."""
+    B, n_kv, d = 3, 2, 16
+    k_new, v_new = kvgen.append_inputs_gqa(B, n_kv, d, seed=21)
+    kn = k_new.view(torch.int16).numpy().view(np.uint16)
+    vn = v_new.view(torch.int16).numpy().view(np.uint16)
+    ks = np.array([0.01, 0.03], np.float32)
+    vs = np.array([0.02, 0.005], np.float32)
+    sl = np.array([5, 0, 131])
+    K = np.zeros((B, n_kv, 192, d), np.uint8)
+    V = np.zeros((B, n_kv, 192, d), np.uint8)
+    K2, V2 = oracle.append_rope_gqa(K, V, sl, kn, vn, k_scale=ks, v_scale=vs)
+    for b in range(B):
+        rot = oracle.rope_rotate(oracle.bf16_bits_to_f64(kn[b]), float(sl[b])) / ks[:, None].astype(np.float64)
+        got = oracle.e4m3_bits_to_f64(K2[b, :, sl[b]])
+        # |x - Q(x)| <= half the gap between the two codes around x
+        mags = oracle.e4m3_bits_to_f64(np.arange(0x7F))
+        hi = np.searchsorted(mags, np.abs(rot))
+        gap = mags[np.minimum(hi, 126)] - mags[np.maximum(hi - 1, 0)]
+        assert np.all(np.abs(got - rot) <= gap / 2 + 1e-15)
+        quot = torch.from_numpy(v_new[b].float().numpy() / vs[:, None])
+        ref = quot.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        np.testing.assert_array_equal(V2[b, :, sl[b]], ref)
+
+
+# ---------------------------------------------------------------- sliding window
+
+def test_window_matches_printed_mask():
+    """window_slots reads exactly the keys the figure marks for w = 4."""
+    g = read_golden("sliding_window_w4.txt")
+    w = 4
+    for t in range(12):
+        slots = oracle.window_slots(t + 1, w)
+        # invert the ring: the position p in (t - w, t] with p mod w == slot
+        pos = sorted(t - ((t - s) % w) for s in slots)
+        mask = np.zeros(12)
+        mask[pos] = 1
+        np.testing.assert_array_equal(mask, g["t%d" % t])
+    # the text's "[t - w, t]" (w + 1 keys) is a different reading
+    assert len(oracle.window_slots(12, w)) == w
+
+
+@pytest.mark.parametrize("paged", [False, True])
+def test_window_ring_equals_last_w_positions(paged):
+    """A ring of w slots holding position p at slot p mod w gives the same
+    decode as plain attention over the last w positions of a linear cache."""
+    w, d, n_kv, h = 37, 8, 2, 4
+    lens = [5, 37, 38, 100, 0]
+    B = len(lens)
+    T = max(lens)
+    q = RNG.normal(size=(B, h, d))
+    Klin = RNG.normal(size=(B, n_kv, T, d))
+    Vlin = RNG.normal(size=(B, n_kv, T, d))
+    Kr = np.zeros((B, n_kv, w, d))
+    Vr = np.zeros((B, n_kv, w, d))
+    for b, n in enumerate(lens):
+        for p in range(max(0, n - w), n):
+            Kr[b, :, p % w] = Klin[b, :, p]
+            Vr[b, :, p % w] = Vlin[b, :, p]
+    bt = None
+    if paged:
+        bt = np.array([[2 * b + 1, 2 * b] for b in range(B)])
+        Kp = np.zeros((2 * B, n_kv, 64, d))
+        Vp = np.zeros((2 * B, n_kv, 64, d))
+        for b in range(B):
+            for s_ in range(w):
+                Kp[bt[b, s_ // 64], :, s_ % 64] = Kr[b, :, s_]
+                Vp[bt[b, s_ // 64], :, s_ % 64] = Vr[b, :, s_]
+        Kr, Vr = Kp, Vp
+    out, lse = oracle.gqa_decode(q, Kr, Vr, np.array(lens), 0.3, bt, window=w)
+    for b, n in enumerate(lens):
+        lo = max(0, n - w)
+        for hh in range(h):
+            o, l = oracle.attend(q[b, hh:hh + 1], Klin[b, hh // 2, lo:n], Vlin[b, hh // 2, lo:n], 0.3)
+            np.testing.assert_allclose(out[b, hh], o[0], atol=1e-12)
+            assert (l[0] == lse[b, hh]) if n == 0 else abs(l[0] - lse[b, hh]) < 1e-12
+    # w >= length: the full decode
+    full, _ = oracle.gqa_decode(q, Klin, Vlin, np.array(lens), 0.3)
+    wide, _ = oracle.gqa_decode(q, Klin, Vlin, np.array(lens), 0.3, window=T)
+    np.testing.assert_array_equal(full, wide)
+
+
+def test_window_append_ring_keeps_last_w():
+    """Appending positions 0..N-1 one by one into a ring of w slots leaves
+    slot s holding the newest position p = s (mod w), rotated to p."""
+    w, n_kv, d, N = 5, 1, 8, 13
+    K = np.zeros((1, n_kv, 8, d), np.uint16)
+    V = np.zeros((1, n_kv, 8, d), np.uint16)
+    ks_, vs_ = [], []
+    for p in range(N):
+        k_new, v_new = kvgen.append_inputs_gqa(1, n_kv, d, seed=100 + p)
+        kn = k_new.view(torch.int16).numpy().view(np.uint16)
+        vn = v_new.view(torch.int16).numpy().view(np.uint16)
+        ks_.append(kn)
+        vs_.append(vn)
+        K, V = oracle.append_rope_gqa(K, V, np.array([p]), kn, vn, window=w)
+    for p in range(N - w, N):
+        rot = oracle.f64_to_bf16_bits(oracle.rope_rotate(oracle.bf16_bits_to_f64(ks_[p][0]), float(p)))
+        np.testing.assert_array_equal(K[0, :, p % w], rot)
+        np.testing.assert_array_equal(V[0, :, p % w], vs_[p][0])
+    assert np.all(K[0, :, w:] == 0)
 
 
 # ---------------------------------------------------------------- closed forms

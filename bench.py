@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--config", default="C1", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="kvdec", choices=["kvdec", "reference"])
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
+                    help="GQA cache element: bf16, or E4M3 bytes with per-KV-head scales")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no CPU baseline, no e2e leg, no clock hold")
@@ -69,7 +71,7 @@ def gqa_bytes(case, out_elem=4):
     """Algorithmic bytes of one decode call: every cached K and V element of
     the attended tokens once, plus q, out, lse and seqlens once."""
     sl = case.seqlens.double().sum().item()
-    kv = sl * case.n_kv * 2 * case.d * 2
+    kv = sl * case.n_kv * 2 * case.d * case.k.element_size()
     q = case.B * case.h * case.d * 2
     out = case.B * case.h * case.d * out_elem + case.B * case.h * 4
     bt = 0 if case.block_table is None else case.block_table.numel() * 4
@@ -77,8 +79,8 @@ def gqa_bytes(case, out_elem=4):
 
 
 def gqa_append_bytes(case):
-    # k_new, v_new read; rotated K row and V row written; positions read
-    return 4 * case.B * case.n_kv * case.d * 2 + case.B * 4
+    # k_new, v_new read (bf16); rotated K row and V row written; positions read
+    return case.B * case.n_kv * case.d * (2 * 2 + 2 * case.k.element_size()) + case.B * 4
 
 
 def mla_bytes(case, out_elem=4):
@@ -342,18 +344,24 @@ def main():
     stream = torch.cuda.current_stream()
     sptr = kvdec._stream(stream)
     mla = args.config.startswith("C3") or args.config.endswith("MLA")
+    if mla and args.kv != "bf16":
+        raise SystemExit("--kv fp8 applies to the GQA workloads")
+    fp8 = args.kv == "fp8"
     hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
 
     # two independent input sets, alternated step by step
     import ctypes
     sets = []
     for rep in range(2):
-        case = kvgen.config_case(args.config, device=dev)
+        case = kvgen.config_case(args.config, device=dev, kv_dtype=args.kv)
         if rep == 1:   # a second, independent draw of the same workload
             g = torch.Generator(device=dev)
             g.manual_seed(7777 + rank)
             if mla:
                 case.cache.copy_(torch.randn(case.cache.shape, generator=g, device=dev).to(torch.bfloat16))
+            elif fp8:
+                case.k.copy_(kvgen.fp8_codes(torch.randn(case.k.shape, generator=g, device=dev), g, dev)[0])
+                case.v.copy_(kvgen.fp8_codes(torch.randn(case.v.shape, generator=g, device=dev), g, dev)[0])
             else:
                 case.k.copy_(torch.randn(case.k.shape, generator=g, device=dev).to(torch.bfloat16))
                 case.v.copy_(torch.randn(case.v.shape, generator=g, device=dev).to(torch.bfloat16))
@@ -384,7 +392,8 @@ def main():
             out = torch.empty(case.q.shape, dtype=torch.float32, device=dev)
             lse = torch.empty(case.q.shape[:2], dtype=torch.float32, device=dev)
             p = kvdec.gqa_params(case.q, case.k, case.v, case.seqlens, case.block_table,
-                                 case.scale, out, lse, None, 0)
+                                 case.scale, out, lse, None, 0, k_scale=case.k_scale,
+                                 v_scale=case.v_scale)
             need = lib.kvdec_gqa_workspace_bytes(ctypes.byref(p))
             wsb = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
             p.workspace, p.workspace_bytes = kvdec._ptr(wsb), wsb.numel()
@@ -400,6 +409,9 @@ def main():
             ap.k_new, ap.v_new = kvdec._ptr(k_new), kvdec._ptr(v_new)
             ap.k, ap.v = kvdec._ptr(case.k), kvdec._ptr(case.v)
             ap.num_kv_heads, ap.head_dim = case.n_kv, case.d
+            if fp8:
+                ap.kv_format = kvdec.KV_FP8_E4M3
+                ap.k_scale, ap.v_scale = kvdec._ptr(case.k_scale), kvdec._ptr(case.v_scale)
             st.update(new=(k_new, v_new), pos=pos, out=out, lse=lse, ws=wsb, p=p, ap=ap,
                       decode=lib.kvdec_gqa_decode)
         sets.append(st)
@@ -467,8 +479,9 @@ def main():
     kfile = ["mla_decode.cu", "common.cuh", "schedule.cuh"] if mla else \
         ["gqa_decode.cu", "common.cuh", "schedule.cuh"]
     kname = "mla_decode_kernel" if mla else "gqa_decode_kernel"
+    tkey = kname + ("[fp8]" if fp8 else "")     # the FP8 instantiation has its own counters
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-            "frac": achieved / hbm_peak, "traffic": ncu_traffic(kname, kfile),
+            "frac": achieved / hbm_peak, "traffic": ncu_traffic(tkey, kfile),
             "kernel": kname, "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
             "algorithmic_bytes_per_launch": dec_alg, "avg_launch_us": dec_avg_ms * 1e3}
     extra = {}
@@ -529,18 +542,23 @@ def main():
     if rank != 0:
         return
     cpu = None
-    if not args.no_cpu_baseline:
+    if fp8:
+        cpu = {"value": None, "note": "no oracle timing for the FP8 cache line; the bf16 "
+                                      "line of the same workload carries it"}
+    elif not args.no_cpu_baseline:
         cpu = cpu_baseline(args.config, args.cpu_seconds)
     cfg = {"workload": WORKLOADS[args.config], "name": args.config,
            "l2": "inputs larger than L2 (KV bytes per step %.0f MB > 126 MB), two input sets "
                  "alternated" % (kv_bytes[0] / 1e6) if kv_bytes[0] > 2 * 126e6 else
                  "KV smaller than 2x L2: two input sets alternated, partly L2-resident",
            "kv_bytes_per_step": kv_bytes[0], "step": "append_rope + decode (fused split merge)",
+           "kv_cache": "E4M3 bytes, per-KV-head fp32 scales" if fp8 else "bf16",
            "parallelism": f"replicas x{ws}"}
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "us_per_step": ms_per_step * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": cfg,
+            "vs_baseline": None, "dtype": "fp8-e4m3 cache, f16 MMA" if fp8 else "bf16",
+            "data": "synthetic", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": 2 * args.steps,
             "append_us": 1e3 * sum(app_ms) / len(app_ms)}

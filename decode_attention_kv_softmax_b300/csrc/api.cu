@@ -103,6 +103,7 @@ kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
 
 struct GqaPlan {
     int D, MT, g, n_hc, hc_rows, units;
+    bool f8;
     int grid;
     size_t off_lse, off_o, bytes;
 };
@@ -125,6 +126,12 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
                     p->num_heads, p->num_kv_heads);
     if (p->head_dim != 64 && p->head_dim != 128)
         return fail(KVDEC_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", p->head_dim);
+    if (p->kv_format != KVDEC_KV_BF16 && p->kv_format != KVDEC_KV_FP8_E4M3)
+        return fail(KVDEC_ERR_INVALID_ARG, "kv_format %d", p->kv_format);
+    pl.f8 = p->kv_format == KVDEC_KV_FP8_E4M3;
+    if (pl.f8 && p->head_dim != 128)
+        return fail(KVDEC_ERR_UNSUPPORTED, "FP8 cache with head_dim %d (supported: 128)", p->head_dim);
+    if (p->window < 0) return fail(KVDEC_ERR_INVALID_ARG, "window %d", p->window);
     pl.D = p->head_dim;
     pl.g = p->num_heads / p->num_kv_heads;
     pl.hc_rows = pl.g <= 32 ? pl.g : 32;
@@ -136,11 +143,11 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
     int occ;
     {
-        auto key = std::make_tuple(dev, 0, pl.D, pl.MT, p->batch);
+        auto key = std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch);
         std::lock_guard<std::mutex> lk(g_mu);
         auto it = g_occupancy.find(key);
         if (it == g_occupancy.end()) {
-            occ = kvdec::occupancy_gqa(pl.D, pl.MT, p->batch);
+            occ = kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, p->batch);
             g_occupancy[key] = occ;
         } else {
             occ = it->second;
@@ -280,10 +287,23 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
     if (rows + KVDEC_PAGE_SIZE >= 0x7fffffffull)
         return fail(KVDEC_ERR_UNSUPPORTED, "cache has %llu rows (limit 2^31 - 64)",
                     (unsigned long long)rows);
+    if (p->window > cap)
+        return fail(KVDEC_ERR_INVALID_ARG, "window %d exceeds the %d cache slots", p->window, cap);
+    if (pl.f8 && (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
+        return fail(KVDEC_ERR_INVALID_ARG, "an FP8 cache needs 4-byte aligned k_scale and v_scale");
     CUtensorMap tk, tv;
-    st = encode_2d(&tk, p->k, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != KVDEC_OK) return st;
-    st = encode_2d(&tv, p->v, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (pl.f8) {
+        // one byte per element: a 64-token box of 128-byte rows
+        st = encode_2d(&tk, p->k, rows, pl.D, (uint64_t)pl.D, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT8);
+        if (st != KVDEC_OK) return st;
+        st = encode_2d(&tv, p->v, rows, pl.D, (uint64_t)pl.D, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    } else {
+        st = encode_2d(&tk, p->k, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (st != KVDEC_OK) return st;
+        st = encode_2d(&tv, p->v, rows, pl.D, (uint64_t)pl.D * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     if (st != KVDEC_OK) return st;
 
     kvdec::GqaArgs a;
@@ -315,7 +335,10 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
     a.scale_log2 = (float)(scale * 1.4426950408889634);
     a.min_tiles = 8;
     a.timeout_ns = kvdec::kDefaultTimeoutNs;
-    cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, tk, tv, a, pl.grid, static_cast<cudaStream_t>(stream));
+    a.k_scale = p->k_scale;
+    a.v_scale = p->v_scale;
+    a.window = p->window;
+    cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, pl.f8, tk, tv, a, pl.grid, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
     return KVDEC_OK;
 }
@@ -459,6 +482,8 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
     if (p->block_table && (p->num_pages < 1 || p->max_blocks < 1))
         return fail(KVDEC_ERR_INVALID_ARG, "paged append needs num_pages >= 1 and max_blocks >= 1");
     if (p->mode == KVDEC_APPEND_MLA) {
+        if (p->kv_format != KVDEC_KV_BF16 || p->window != 0)
+            return fail(KVDEC_ERR_UNSUPPORTED, "MLA append takes neither kv_format nor window");
         if (!p->block_table || !p->c_kv || !p->k_rope || !p->cache)
             return fail(KVDEC_ERR_INVALID_ARG, "MLA append needs block_table, c_kv, k_rope and cache");
         if (!aligned(p->c_kv, 16) || !aligned(p->cache, 16) || !aligned(p->k_rope, 4))
@@ -478,11 +503,23 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
             return fail(KVDEC_ERR_INVALID_ARG, "contiguous append needs capacity >= 1");
         if (!aligned(p->v_new, 16) || !aligned(p->v, 16) || !aligned(p->k_new, 4) || !aligned(p->k, 4))
             return fail(KVDEC_ERR_INVALID_ARG, "v_new and v must be 16-byte aligned");
+        if (p->kv_format != KVDEC_KV_BF16 && p->kv_format != KVDEC_KV_FP8_E4M3)
+            return fail(KVDEC_ERR_INVALID_ARG, "kv_format %d", p->kv_format);
+        a.fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
+        if (a.fp8 && (!p->k_scale || !p->v_scale || !aligned(p->k_scale, 4) || !aligned(p->v_scale, 4)))
+            return fail(KVDEC_ERR_INVALID_ARG, "an FP8 cache needs 4-byte aligned k_scale and v_scale");
+        const int slots = p->block_table ? p->max_blocks * KVDEC_PAGE_SIZE : p->capacity;
+        if (p->window < 0 || p->window > slots)
+            return fail(KVDEC_ERR_INVALID_ARG, "window %d (must be 0 or at most the %d cache slots)",
+                        p->window, slots);
+        a.window = p->window;
+        a.k_scale = p->k_scale;
+        a.v_scale = p->v_scale;
         a.mode = 1;
         a.k_new = static_cast<const __nv_bfloat16*>(p->k_new);
         a.v_new = static_cast<const __nv_bfloat16*>(p->v_new);
-        a.k = static_cast<__nv_bfloat16*>(p->k);
-        a.v = static_cast<__nv_bfloat16*>(p->v);
+        a.k = p->k;
+        a.v = p->v;
         a.n_kv = p->num_kv_heads;
         a.d = p->head_dim;
         a.cap = p->capacity;

@@ -11,14 +11,19 @@
 // in binary64), the sine/cosine of the reduced angle and the rotation in
 // binary32, and the result is rounded once to bf16 (nearest-even).  The kernel moves a few KB per call: it is launch-latency
 // bound, so it is written for simplicity, one CTA per (sequence, head).
+//
+// GQA options: an FP8 cache ([ARG] §六.3) stores E4M3(x / scale[kv head])
+// (nearest-even, saturating at 448; the quotient is the correctly rounded
+// binary32 one), and a sliding window of w tokens ([ARG] §五.3) writes the
+// ring slot pos mod w while the rotation keeps the position pos.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace kvdec {
 
 
-KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int pos,
-                            const double* inv_freq) {
+// Rotated pair i of x at position pos, in binary32.
+KVDEC_DEVINL float2 rope_pair_f32(const __nv_bfloat16* x, int i, int pos, const double* inv_freq) {
     // angle in binary64, reduced to [-pi, pi] in binary64, then sine/cosine
     // and the rotation in binary32 (|error| ~1e-7, far below one bf16 ulp)
     const double ang = (double)pos * inv_freq[i];
@@ -27,13 +32,25 @@ KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int
     sincosf((float)r, &s, &c);
     const float x0 = __bfloat162float(x[2 * i]);
     const float x1 = __bfloat162float(x[2 * i + 1]);
-    y[2 * i] = __float2bfloat16_rn(fmaf(x0, c, -x1 * s));
-    y[2 * i + 1] = __float2bfloat16_rn(fmaf(x0, s, x1 * c));
+    return make_float2(fmaf(x0, c, -x1 * s), fmaf(x0, s, x1 * c));
+}
+
+KVDEC_DEVINL void rope_pair(const __nv_bfloat16* x, __nv_bfloat16* y, int i, int pos,
+                            const double* inv_freq) {
+    const float2 r = rope_pair_f32(x, i, pos, inv_freq);
+    y[2 * i] = __float2bfloat16_rn(r.x);
+    y[2 * i + 1] = __float2bfloat16_rn(r.y);
+}
+
+KVDEC_DEVINL uint8_t to_e4m3(float x) {
+    return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
 }
 
 __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
     const int b = blockIdx.x, head = blockIdx.y, t = threadIdx.x;
-    const int pos = __ldg(a.seqlens + b);
+    const int pos_abs = __ldg(a.seqlens + b);
+    // ring slot of a sliding-window cache; the rotation uses pos_abs
+    const int pos = (a.window > 0 && pos_abs >= 0) ? pos_abs % a.window : pos_abs;
     const int cap = a.block_table ? a.max_blocks * KVDEC_PAGE_SIZE : a.cap;
     if (pos < 0 || pos >= cap) {
         if (t == 0 && head == 0) report(a.err, KVDEC_DEVERR_SEQLEN);
@@ -62,9 +79,24 @@ __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
     size_t dst_off;
     if (a.block_table) dst_off = (((size_t)page * a.n_kv + head) * KVDEC_PAGE_SIZE + slot) * a.d;
     else dst_off = (((size_t)b * a.n_kv + head) * a.cap + pos) * a.d;
-    if (t < a.d / 2) rope_pair(a.k_new + src_off, a.k + dst_off, t, pos, a.inv_freq);
+    if (a.fp8) {
+        uint8_t* k8 = static_cast<uint8_t*>(a.k) + dst_off;
+        uint8_t* v8 = static_cast<uint8_t*>(a.v) + dst_off;
+        const float ks = __ldg(a.k_scale + head), vs = __ldg(a.v_scale + head);
+        if (t < a.d / 2) {
+            const float2 r = rope_pair_f32(a.k_new + src_off, t, pos_abs, a.inv_freq);
+            k8[2 * t] = to_e4m3(__fdiv_rn(r.x, ks));
+            k8[2 * t + 1] = to_e4m3(__fdiv_rn(r.y, ks));
+        }
+        for (int i = t; i < a.d; i += blockDim.x)
+            v8[i] = to_e4m3(__fdiv_rn(__bfloat162float(a.v_new[src_off + i]), vs));
+        return;
+    }
+    __nv_bfloat16* k16 = static_cast<__nv_bfloat16*>(a.k);
+    __nv_bfloat16* v16 = static_cast<__nv_bfloat16*>(a.v);
+    if (t < a.d / 2) rope_pair(a.k_new + src_off, k16 + dst_off, t, pos_abs, a.inv_freq);
     if (t < a.d / 8)
-        reinterpret_cast<uint4*>(a.v + dst_off)[t] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src_off) + t);
+        reinterpret_cast<uint4*>(v16 + dst_off)[t] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src_off) + t);
 }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {

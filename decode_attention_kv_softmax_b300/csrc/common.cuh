@@ -5,6 +5,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -282,6 +283,35 @@ KVDEC_DEVINL void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// f16 inputs, fp32 accumulation (the FP8 path: E4M3 widens exactly to f16)
+KVDEC_DEVINL void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+KVDEC_DEVINL uint32_t ld_shared_u32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// Two E4M3 codes (bits 0-7 the first, 8-15 the second) -> f16x2 (first in the
+// low half).  Exact: every E4M3 value, subnormals included, is an f16 number.
+KVDEC_DEVINL uint32_t e4m3x2_to_f16x2(uint32_t codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+// bf16x2 -> f16x2 (exact for |x| in f16's normal range)
+KVDEC_DEVINL uint32_t bf16x2_to_f16x2(uint32_t u) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 // ---------------------------------------------------------------- numerics

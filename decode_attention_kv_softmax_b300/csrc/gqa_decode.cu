@@ -21,6 +21,19 @@
 //    streams the same number of tiles; pieces of a (b, kv head) unit that
 //    cross CTAs are merged by log-sum-exp ([ARG] §五.2) in the same kernel by
 //    the last CTA to finish the unit.
+//  * FP8 cache (F8, [ARG] §六.3: E4M3 halves the bytes per element, one scale
+//    per head): the tiles arrive as 8-bit codes, half the bytes, and the
+//    MMAs run in f16, to which every E4M3 value widens exactly.  K: ldmatrix
+//    on the 8-bit rows hands a thread 4 consecutive dims of one token, so
+//    the contraction order inside each 16-dim step is permuted (thread t
+//    holds dims 4t..4t+3) and the Q fragments are loaded in that order.  V:
+//    each thread reads one 32-bit word (4 dims) from each of its 4 tokens,
+//    and a byte permute pairs the tokens per dim, giving the B fragment of
+//    dim 4g+i for output tile i; the output columns are mapped back at the
+//    flush.  The K scale folds into the softmax scale, the V scale into the
+//    final normalisation.
+//  * Sliding window ([ARG] §五.3): with a ring cache of w slots a step reads
+//    the min(seqlen, w) slots holding the last w tokens (read_len).
 #include "common.cuh"
 #include "kernels.h"
 #include "schedule.cuh"
@@ -28,10 +41,11 @@
 namespace kvdec {
 
 
-template <int D, int MT, int NS>
+template <int D, int MT, int NS, bool F8>
 struct GqaSmem {
     static constexpr int kBoxBytes = 64 * 128;                // 64 rows x 128 B
-    static constexpr int kBoxes = D / 64;
+    static constexpr int kBoxElems = F8 ? 128 : 64;           // elements per box row
+    static constexpr int kBoxes = D / kBoxElems;
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRows = 16 * MT;
@@ -46,11 +60,12 @@ struct GqaSmem {
     static constexpr int bytes(int B) { return kCum + (B + 1) * 4 + 1024; }
 };
 
-template <int D, int MT, int NS>
+template <int D, int MT, int NS, bool F8>
 __global__ void __launch_bounds__(160, 2)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const GqaArgs a) {
-    using L = GqaSmem<D, MT, NS>;
+    static_assert(!F8 || D == 128, "the FP8 path is built for head_dim 128");
+    using L = GqaSmem<D, MT, NS, F8>;
     constexpr int ROWS = L::kRows;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -74,7 +89,7 @@ __global__ void __launch_bounds__(160, 2)
         misc[1] = 0;
         fence_barrier_init();
     }
-    build_cum(cum, scratch, a.seqlens, a.B, a.cap, a.err);
+    build_cum(cum, scratch, a.seqlens, a.B, a.cap, a.err, a.window);
 
     TileSchedule S;
     S.cum = cum;
@@ -118,8 +133,8 @@ __global__ void __launch_bounds__(160, 2)
             const uint32_t dst = smem_addr(smem + stage * L::kStageBytes);
 #pragma unroll
             for (int x = 0; x < L::kBoxes; ++x) {
-                tma_load_2d(dst + x * L::kBoxBytes, &tmK, fb, x * 64, row, pol);
-                tma_load_2d(dst + L::kTileBytes + x * L::kBoxBytes, &tmV, fb, x * 64, row, pol);
+                tma_load_2d(dst + x * L::kBoxBytes, &tmK, fb, x * L::kBoxElems, row, pol);
+                tma_load_2d(dst + L::kTileBytes + x * L::kBoxBytes, &tmV, fb, x * L::kBoxElems, row, pol);
             }
             ++issued;
             if (++stage == NS) {
@@ -179,17 +194,18 @@ __global__ void __launch_bounds__(160, 2)
     float m[2], l[2];
     int len = 0, nrows = 0;
     bool seg_start = true, seg_item_first = true, seg_unit_first = true;
-    const float sl2 = a.scale_log2;
+    float sl2 = a.scale_log2;
 
     for (long long t = t_begin; t < t_end; ++t) {
         if (seg_start) {
             seg_start = false;
             seg_item_first = (t == t_begin);
             seg_unit_first = (cur.lt == 0);
-            len = clamp_len(__ldg(a.seqlens + cur.b), a.cap, nullptr);
+            len = read_len(__ldg(a.seqlens + cur.b), a.window, a.cap, nullptr);
             const int kvh = cur.j / a.n_hc, hc = cur.j % a.n_hc;
             nrows = min(a.hc_rows, a.g - hc * a.hc_rows);
             const int h0 = kvh * a.g + hc * a.hc_rows;
+            if (F8) sl2 = a.scale_log2 * __ldg(a.k_scale + kvh);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int r = 16 * mt_w + quad + 8 * half;
@@ -198,8 +214,16 @@ __global__ void __launch_bounds__(160, 2)
                 const bool ok = r < nrows;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    qa[ks][half] = ok ? __ldg(qrow + ks * 8 + qc) : 0u;
-                    qa[ks][half + 2] = ok ? __ldg(qrow + ks * 8 + 4 + qc) : 0u;
+                    if (F8) {
+                        // dims 16 ks + 4 qc .. +3, in the order the K fragments use
+                        const uint2 u = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 8 + 2 * qc))
+                                           : make_uint2(0u, 0u);
+                        qa[ks][half] = bf16x2_to_f16x2(u.x);
+                        qa[ks][half + 2] = bf16x2_to_f16x2(u.y);
+                    } else {
+                        qa[ks][half] = ok ? __ldg(qrow + ks * 8 + qc) : 0u;
+                        qa[ks][half + 2] = ok ? __ldg(qrow + ks * 8 + 4 + qc) : 0u;
+                    }
                 }
             }
             m[0] = m[1] = -INFINITY;
@@ -219,13 +243,28 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t tok = tok_base + nt * 8 + (lane & 7);
+                if constexpr (F8) {
+                    // 8-bit rows of 128 dims: matrix i of the x4 load is the
+                    // 16-dim step 4 kk + i; a thread gets dims 4 qc .. 4 qc + 3
 #pragma unroll
-                for (int kk = 0; kk < D / 32; ++kk) {
-                    const uint32_t chunk = 4 * kk + (lane >> 3);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
-                    mma_bf16_16816(s[nt], qa[2 * kk], r0, r1);
-                    mma_bf16_16816(s[nt], qa[2 * kk + 1], r2, r3);
+                    for (int kk = 0; kk < D / 64; ++kk) {
+                        const uint32_t chunk = 4 * kk + (lane >> 3);
+                        uint32_t r[4];
+                        ldsm_x4(kb + swz128(tok, chunk), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i)
+                            mma_f16_16816(s[nt], qa[4 * kk + i], e4m3x2_to_f16x2(r[i]),
+                                          e4m3x2_to_f16x2(r[i] >> 16));
+                    }
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 32; ++kk) {
+                        const uint32_t chunk = 4 * kk + (lane >> 3);
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(kb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
+                        mma_bf16_16816(s[nt], qa[2 * kk], r0, r1);
+                        mma_bf16_16816(s[nt], qa[2 * kk + 1], r2, r3);
+                    }
                 }
             }
             const bool partial = n_valid < kTileTokens;
@@ -264,8 +303,8 @@ __global__ void __launch_bounds__(160, 2)
                 const float p3 = fast_exp2(fmaf(s[nt][3], sl2, -b1));
                 ps0 += p0 + p1;
                 ps1 += p2 + p3;
-                pa[nt >> 1][(nt & 1) * 2 + 0] = pack_bf16x2(p0, p1);
-                pa[nt >> 1][(nt & 1) * 2 + 1] = pack_bf16x2(p2, p3);
+                pa[nt >> 1][(nt & 1) * 2 + 0] = F8 ? pack_half2(p0, p1) : pack_bf16x2(p0, p1);
+                pa[nt >> 1][(nt & 1) * 2 + 1] = F8 ? pack_half2(p2, p3) : pack_bf16x2(p2, p3);
             }
             l[0] = fmaf(l[0], al0, ps0);
             l[1] = fmaf(l[1], al1, ps1);
@@ -282,6 +321,33 @@ __global__ void __launch_bounds__(160, 2)
                 const int tk = tok_base + 16 * ks + 2 * qc;
                 const uint32_t keep_lo = (tk < n_valid ? 0x0000ffffu : 0u) | (tk + 1 < n_valid ? 0xffff0000u : 0u);
                 const uint32_t keep_hi = (tk + 8 < n_valid ? 0x0000ffffu : 0u) | (tk + 9 < n_valid ? 0xffff0000u : 0u);
+                if constexpr (F8) {
+                    // tokens tk, tk+1, tk+8, tk+9 (the B fragment's k rows);
+                    // per 32-dim block c a thread reads dims 32 c + 4 quad .. +3
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        const uint32_t chunk = 2 * c + (quad >> 2), sub = 4 * (quad & 3);
+                        const uint32_t w0 = ld_shared_u32(vb + swz128(tk, chunk) + sub);
+                        const uint32_t w1 = ld_shared_u32(vb + swz128(tk + 1, chunk) + sub);
+                        const uint32_t w2 = ld_shared_u32(vb + swz128(tk + 8, chunk) + sub);
+                        const uint32_t w3 = ld_shared_u32(vb + swz128(tk + 9, chunk) + sub);
+                        // byte pairs per dim: lo word (dims 0, 1), hi word (dims 2, 3)
+                        const uint32_t p01[2] = {__byte_perm(w0, w1, 0x5140), __byte_perm(w0, w1, 0x7362)};
+                        const uint32_t p23[2] = {__byte_perm(w2, w3, 0x5140), __byte_perm(w2, w3, 0x7362)};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int sh = 16 * (i & 1);
+                            uint32_t b0 = e4m3x2_to_f16x2(p01[i >> 1] >> sh);
+                            uint32_t b1 = e4m3x2_to_f16x2(p23[i >> 1] >> sh);
+                            if (partial) {
+                                b0 &= keep_lo;
+                                b1 &= keep_hi;
+                            }
+                            mma_f16_16816(o[4 * c + i], pa[ks], b0, b1);
+                        }
+                    }
+                    continue;
+                }
 #pragma unroll
                 for (int nd2 = 0; nd2 < D / 16; ++nd2) {
                     const int mat = lane >> 3;
@@ -343,7 +409,25 @@ __global__ void __launch_bounds__(160, 2)
                     for (int r = 0; r < 2; ++r) {
                         const int row = 16 * mt_w + quad + 8 * r;
                         const float M = rowml[row * 2];
-                        const float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
+                        float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
+                        if constexpr (F8) {
+                            // FP8: output tile nd = 4 c + i holds dims 32 c + 8 qc + i (+4)
+                            sc *= __ldg(a.v_scale + kvh);
+                            float* dst = obuf + row * L::kOStride + 8 * qc;
+#pragma unroll
+                            for (int nd = 0; nd < D / 8; ++nd) {
+                                float* p0 = dst + 32 * (nd >> 2) + (nd & 3);
+                                const float v0 = o[nd][2 * r] * sc, v1 = o[nd][2 * r + 1] * sc;
+                                if (step == 0) {
+                                    p0[0] = v0;
+                                    p0[4] = v1;
+                                } else {
+                                    p0[0] += v0;
+                                    p0[4] += v1;
+                                }
+                            }
+                            continue;
+                        }
                         float* dst = obuf + row * L::kOStride + 2 * qc;
 #pragma unroll
                         for (int nd = 0; nd < D / 8; ++nd) {
@@ -458,23 +542,23 @@ __global__ void __launch_bounds__(160, 2)
 
 // ---------------------------------------------------------------- launcher
 
-template <int D, int MT, int NS>
+template <int D, int MT, int NS, bool F8>
 static cudaError_t launch_gqa_t(const CUtensorMap& tk, const CUtensorMap& tv, const GqaArgs& a,
                                 int grid, cudaStream_t st) {
-    using L = GqaSmem<D, MT, NS>;
+    using L = GqaSmem<D, MT, NS, F8>;
     const int smem = L::bytes(a.B);
-    auto kern = gqa_decode_kernel<D, MT, NS>;
+    auto kern = gqa_decode_kernel<D, MT, NS, F8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, 160, smem, st>>>(tk, tv, a);
     return cudaGetLastError();
 }
 
-template <int D, int MT, int NS>
+template <int D, int MT, int NS, bool F8>
 static int occupancy_gqa_t(int B) {
-    using L = GqaSmem<D, MT, NS>;
+    using L = GqaSmem<D, MT, NS, F8>;
     const int smem = L::bytes(B);
-    auto kern = gqa_decode_kernel<D, MT, NS>;
+    auto kern = gqa_decode_kernel<D, MT, NS, F8>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
         return 0;
     int n = 0;
@@ -482,17 +566,19 @@ static int occupancy_gqa_t(int B) {
     return n;
 }
 
-// Stages per configuration: a 64-token K+V tile is 32 KB at D=128, 16 KB at
-// D=64; three (six) of them keep ~96 KB in flight per CTA, two CTAs per SM.
-#define KVDEC_GQA_DISPATCH(FN, ...)                                        \
-    (D == 128 ? (MT == 1 ? FN<128, 1, 3>(__VA_ARGS__) : FN<128, 2, 3>(__VA_ARGS__)) \
-              : (MT == 1 ? FN<64, 1, 6>(__VA_ARGS__) : FN<64, 2, 6>(__VA_ARGS__)))
+// Stages per configuration: a 64-token K+V tile is 32 KB at D=128 (16 KB
+// with the FP8 cache), 16 KB at D=64; three (six) of them keep ~96 KB in
+// flight per CTA, two CTAs per SM.
+#define KVDEC_GQA_DISPATCH(FN, ...)                                                          \
+    (F8 ? (MT == 1 ? FN<128, 1, 6, true>(__VA_ARGS__) : FN<128, 2, 6, true>(__VA_ARGS__))  \
+        : D == 128 ? (MT == 1 ? FN<128, 1, 3, false>(__VA_ARGS__) : FN<128, 2, 3, false>(__VA_ARGS__)) \
+                   : (MT == 1 ? FN<64, 1, 6, false>(__VA_ARGS__) : FN<64, 2, 6, false>(__VA_ARGS__)))
 
-cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st) {
     return KVDEC_GQA_DISPATCH(launch_gqa_t, tk, tv, a, grid, st);
 }
 
-int occupancy_gqa(int D, int MT, int B) { return KVDEC_GQA_DISPATCH(occupancy_gqa_t, B); }
+int occupancy_gqa(int D, int MT, bool F8, int B) { return KVDEC_GQA_DISPATCH(occupancy_gqa_t, B); }
 
 }  // namespace kvdec

@@ -24,6 +24,10 @@ struct GqaArgs {
     float scale_log2;
     int min_tiles;
     uint64_t timeout_ns;
+    // E4M3 cache: per-KV-head fp32 scales (dequantised value = code * scale)
+    const float* k_scale;
+    const float* v_scale;
+    int window;          // > 0: ring cache of the last `window` tokens
 };
 
 struct CombineArgs {
@@ -50,10 +54,14 @@ struct AppendArgs {
     __nv_bfloat16* cache;
     const __nv_bfloat16* k_new;
     const __nv_bfloat16* v_new;
-    __nv_bfloat16* k;
-    __nv_bfloat16* v;
+    void* k;             // bf16, or E4M3 bytes when fp8
+    void* v;
     int n_kv, d, cap;
     uint32_t* err;
+    int fp8;             // GQA: E4M3 cache with per-KV-head scales
+    int window;          // GQA: > 0 ring cache of `window` slots
+    const float* k_scale;
+    const float* v_scale;
 };
 
 struct MlaMaps {
@@ -93,9 +101,9 @@ cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStr
 cudaError_t launch_mla_proj(bool absorb, const MlaProjArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
 
-cudaError_t launch_gqa(int D, int MT, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st);
-int occupancy_gqa(int D, int MT, int B);
+int occupancy_gqa(int D, int MT, bool F8, int B);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* err, cudaStream_t st);

@@ -105,18 +105,28 @@ KVDEC_DEVINL int clamp_len(int len, int cap, uint32_t* err) {
     return len;
 }
 
-// Block-wide: cum[0..B] from seqlens (clamped to cap).  `scratch` holds
+// Tokens one decode step reads from the cache: every one of the sequence's
+// len tokens, or with a sliding window of w tokens kept in a ring cache of w
+// slots ([ARG] "attention-variants-and-kv-cache" §五.3) the min(len, w)
+// slots that hold the last w positions (softmax does not depend on their
+// order).  Clamped to the capacity like the plain length.
+KVDEC_DEVINL int read_len(int len, int window, int cap, uint32_t* err) {
+    if (window > 0 && len > window) len = window;
+    return clamp_len(len, cap, err);
+}
+
+// Block-wide: cum[0..B] from seqlens (read_len of each).  `scratch` holds
 // blockDim.x ints.  Each thread sums a contiguous chunk of
 // sequences, warp 0 scans the per-thread sums with shuffles, and each thread
 // writes its chunk's prefix.  Ends with __syncthreads().
 KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int B, int cap,
-                            uint32_t* err) {
+                            uint32_t* err, int window = 0) {
     const int tid = threadIdx.x, nth = blockDim.x;
     const int chunk = (B + nth - 1) / nth;
     const int lo = min(B, tid * chunk), hi = min(B, lo + chunk);
     int sum = 0;
     for (int b = lo; b < hi; ++b) {
-        const int len = clamp_len(__ldg(seqlens + b), cap, blockIdx.x == 0 ? err : nullptr);
+        const int len = read_len(__ldg(seqlens + b), window, cap, blockIdx.x == 0 ? err : nullptr);
         sum += (len + kTileTokens - 1) / kTileTokens;
     }
     scratch[tid] = sum;
@@ -145,7 +155,7 @@ KVDEC_DEVINL void build_cum(int* cum, int* scratch, const int32_t* seqlens, int 
     int run = scratch[tid];
     for (int b = lo; b < hi; ++b) {
         cum[b] = run;
-        const int len = clamp_len(__ldg(seqlens + b), cap, nullptr);
+        const int len = read_len(__ldg(seqlens + b), window, cap, nullptr);
         run += (len + kTileTokens - 1) / kTileTokens;
     }
     __syncthreads();

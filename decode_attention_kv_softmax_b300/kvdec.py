@@ -17,7 +17,9 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvdec.so")
 
+ABI_VERSION = 2
 F32, BF16 = 0, 1
+KV_BF16, KV_FP8_E4M3 = 0, 1
 APPEND_MLA, APPEND_GQA = 0, 1
 DEVERR_BAD_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 0x1, 0x2, 0x4
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "CUDA error",
@@ -32,7 +34,8 @@ class GqaParams(ctypes.Structure):
                 ("max_blocks", c_int32), ("scale", c_float), ("out", c_void_p),
                 ("out_dtype", c_int32), ("lse", c_void_p), ("workspace", c_void_p),
                 ("workspace_bytes", c_size_t), ("error_flag", c_void_p),
-                ("max_ctas", c_int32), ("reserved", c_int32)]
+                ("max_ctas", c_int32), ("kv_format", c_int32), ("k_scale", c_void_p),
+                ("v_scale", c_void_p), ("window", c_int32), ("reserved", c_int32)]
 
 
 class MlaParams(ctypes.Structure):
@@ -51,7 +54,8 @@ class AppendParams(ctypes.Structure):
                 ("cache", c_void_p), ("k_new", c_void_p), ("v_new", c_void_p),
                 ("k", c_void_p), ("v", c_void_p), ("num_kv_heads", c_int32),
                 ("head_dim", c_int32), ("capacity", c_int32), ("reserved", c_int32),
-                ("error_flag", c_void_p)]
+                ("error_flag", c_void_p), ("kv_format", c_int32), ("window", c_int32),
+                ("k_scale", c_void_p), ("v_scale", c_void_p)]
 
 
 class CombineParams(ctypes.Structure):
@@ -108,7 +112,7 @@ def load(path: str = LIB_PATH):
             f.argtypes = [ctypes.POINTER(st), c_void_p]
         lib.kvdec_selftest_wait_timeout.restype = ctypes.c_int
         lib.kvdec_selftest_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
-        if lib.kvdec_abi_version() != 1:
+        if lib.kvdec_abi_version() != ABI_VERSION:
             raise RuntimeError("libkvdec ABI version mismatch")
         for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams, MlaProjParams]):
             if lib.kvdec_params_size(kind) != ctypes.sizeof(st):
@@ -193,9 +197,35 @@ def new_error_flag(device=None) -> torch.Tensor:
 
 # ---------------------------------------------------------------- GQA
 
+_FP8_DTYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def _kv_format(k, v, k_scale, v_scale, dev) -> int:
+    """KV_BF16 for a bf16 cache; KV_FP8_E4M3 for E4M3 bytes (uint8 or
+    float8_e4m3fn) with fp32 per-KV-head scales on the same device."""
+    if k.dtype == torch.bfloat16:
+        _need(v, "v", torch.bfloat16, dev)
+        return KV_BF16
+    if k.dtype not in _FP8_DTYPES or v.dtype not in _FP8_DTYPES:
+        raise TypeError(f"k, v must be bf16 or E4M3 bytes, got {k.dtype}, {v.dtype}")
+    if k_scale is None or v_scale is None:
+        raise ValueError("an FP8 cache needs k_scale and v_scale")
+    n_kv = k.shape[1]
+    for t, n in [(k_scale, "k_scale"), (v_scale, "v_scale")]:
+        _need(t, n, torch.float32, dev)
+        if t.numel() != n_kv:
+            raise ValueError(f"{n} must hold num_kv_heads={n_kv} values")
+    return KV_FP8_E4M3
+
+
 def gqa_params(q, k, v, seqlens, block_table=None, scale=None, out=None, lse=None,
-               error_flag=None, max_ctas=0, workspace=None):
+               error_flag=None, max_ctas=0, workspace=None, k_scale=None, v_scale=None,
+               window=0):
     p = GqaParams()
+    if k.dtype in _FP8_DTYPES:
+        p.kv_format = KV_FP8_E4M3
+        p.k_scale, p.v_scale = _ptr(k_scale), _ptr(v_scale)
+    p.window = int(window)
     B, H, D = q.shape
     p.q, p.k, p.v = _ptr(q), _ptr(k), _ptr(v)
     p.block_table = _ptr(block_table)
@@ -219,9 +249,9 @@ def gqa_params(q, k, v, seqlens, block_table=None, scale=None, out=None, lse=Non
     return p
 
 
-def gqa_workspace_bytes(q, k, v, seqlens, block_table=None, max_ctas=0) -> int:
+def gqa_workspace_bytes(q, k, v, seqlens, block_table=None, max_ctas=0, window=0) -> int:
     lib = load()
-    p = gqa_params(q, k, v, seqlens, block_table, max_ctas=max_ctas)
+    p = gqa_params(q, k, v, seqlens, block_table, max_ctas=max_ctas, window=window)
     n = lib.kvdec_gqa_workspace_bytes(ctypes.byref(p))
     if n == 0:
         raise KvdecError("kvdec_gqa_workspace_bytes: " + lib.kvdec_last_error().decode())
@@ -230,14 +260,17 @@ def gqa_workspace_bytes(q, k, v, seqlens, block_table=None, max_ctas=0) -> int:
 
 def gqa_decode(q, k, v, seqlens, block_table=None, scale=None, out_dtype=torch.float32,
                out=None, return_lse=True, error_flag=None, max_ctas=0, workspace=None,
-               stream=None):
+               stream=None, k_scale=None, v_scale=None, window=0):
     """MHA/GQA/MQA decode.  q [B,h,d] bf16; k, v contiguous [B,n_kv,cap,d] or
-    paged [pages,n_kv,64,d] bf16 (with block_table [B,max_blocks] int32);
-    seqlens [B] int32.  Returns (out [B,h,d], lse [B,h] or None)."""
+    paged [pages,n_kv,64,d] (with block_table [B,max_blocks] int32), bf16 or
+    E4M3 bytes with fp32 k_scale, v_scale [n_kv]; seqlens [B] int32;
+    window > 0 reads a ring cache of the last ``window`` tokens.  Returns
+    (out [B,h,d], lse [B,h] or None)."""
     lib = load()
     dev = q.device
-    for t, n in [(q, "q"), (k, "k"), (v, "v")]:
-        _need(t, n, torch.bfloat16, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", k.dtype, dev)
+    _kv_format(k, v, k_scale, v_scale, dev)
     _need(seqlens, "seqlens", torch.int32, dev)
     if block_table is not None:
         _need(block_table, "block_table", torch.int32, dev)
@@ -246,7 +279,8 @@ def gqa_decode(q, k, v, seqlens, block_table=None, scale=None, out_dtype=torch.f
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=dev)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
-    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas)
+    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas,
+                   k_scale=k_scale, v_scale=v_scale, window=window)
     need = lib.kvdec_gqa_workspace_bytes(ctypes.byref(p))
     if need == 0:
         raise KvdecError("kvdec_gqa_decode: " + lib.kvdec_last_error().decode())
@@ -260,7 +294,7 @@ def gqa_decode(q, k, v, seqlens, block_table=None, scale=None, out_dtype=torch.f
 
 def gqa_decode_noalloc(q, k, v, seqlens, block_table=None, scale=None,
                        out_dtype=torch.float32, out=None, return_lse=True, error_flag=None,
-                       max_ctas=0, stream=None):
+                       max_ctas=0, stream=None, k_scale=None, v_scale=None, window=0):
     """kvdec_gqa_decode_noalloc: the same decode for callers that cannot
     allocate device memory; the library keeps the split scratch in its own
     fixed 16 MiB array per GPU, so only inputs and outputs are passed (the
@@ -268,15 +302,17 @@ def gqa_decode_noalloc(q, k, v, seqlens, block_table=None, scale=None,
     library).  Calls sharing a device must not overlap on the GPU."""
     lib = load()
     dev = q.device
-    for t, n in [(q, "q"), (k, "k"), (v, "v")]:
-        _need(t, n, torch.bfloat16, dev)
+    _need(q, "q", torch.bfloat16, dev)
+    _need(k, "k", k.dtype, dev)
+    _kv_format(k, v, k_scale, v_scale, dev)
     _need(seqlens, "seqlens", torch.int32, dev)
     if block_table is not None:
         _need(block_table, "block_table", torch.int32, dev)
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=dev)
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
-    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas)
+    p = gqa_params(q, k, v, seqlens, block_table, scale, out, lse, error_flag, max_ctas,
+                   k_scale=k_scale, v_scale=v_scale, window=window)
     _check(lib.kvdec_gqa_decode_noalloc(ctypes.byref(p), _stream(stream)),
            "kvdec_gqa_decode_noalloc")
     return out, lse
@@ -353,16 +389,24 @@ def append_rope_mla(cache, block_table, seqlens, c_kv, k_rope, rope_theta=10000.
 
 
 def append_rope_gqa(k, v, seqlens, k_new, v_new, block_table=None, rope_theta=10000.0,
-                    error_flag=None, stream=None):
-    """K[.., pos, :] = RoPE_pos(k_new), V[.., pos, :] = v_new at pos =
-    seqlens[b] (in place), contiguous or paged caches."""
+                    error_flag=None, stream=None, k_scale=None, v_scale=None, window=0):
+    """K[.., slot, :] = RoPE_pos(k_new), V[.., slot, :] = v_new at pos =
+    seqlens[b] (in place), contiguous or paged caches; slot = pos, or pos mod
+    window for a ring cache.  E4M3 caches (uint8 / float8_e4m3fn k, v) store
+    the codes of the values divided by k_scale / v_scale [n_kv]."""
     lib = load()
     dev = k.device
-    for t, n in [(k, "k"), (v, "v"), (k_new, "k_new"), (v_new, "v_new")]:
+    for t, n in [(k_new, "k_new"), (v_new, "v_new")]:
         _need(t, n, torch.bfloat16, dev)
+    _need(k, "k", k.dtype, dev)
+    fmt = _kv_format(k, v, k_scale, v_scale, dev)
     _need(seqlens, "seqlens", torch.int32, dev)
     p = AppendParams()
     p.mode = APPEND_GQA
+    p.kv_format = fmt
+    p.window = int(window)
+    if fmt == KV_FP8_E4M3:
+        p.k_scale, p.v_scale = _ptr(k_scale), _ptr(v_scale)
     p.batch = k_new.shape[0]
     p.seqlens = _ptr(seqlens)
     if block_table is not None:

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVDEC_ABI_VERSION 1
+#define KVDEC_ABI_VERSION 2
 #define KVDEC_PAGE_SIZE 64      /* tokens per KV page (block) */
 #define KVDEC_MLA_DC 512        /* MLA latent width d_c */
 #define KVDEC_MLA_DR 64         /* MLA decoupled rope key width d_h^R */
@@ -61,6 +61,14 @@ typedef enum kvdec_status {
 #define KVDEC_DEVERR_TIMEOUT 0x4u    /* a bounded device wait ran out */
 
 typedef enum kvdec_dtype { KVDEC_F32 = 0, KVDEC_BF16 = 1 } kvdec_dtype;
+
+/* Element format of a GQA K/V cache ([ARG] §六.3: quantising the cache to
+ * FP8 E4M3 halves the bytes per element, with one scale per head or per
+ * token).  KVDEC_KV_FP8_E4M3: every K and V element is one E4M3 byte (the
+ * format of "FP8 Formats for Deep Learning", Micikevicius et al. 2022), and
+ * the value it stands for is E4M3(code) * scale[kv head], with one fp32 scale
+ * per KV head for K and one for V. */
+typedef enum kvdec_kv_format { KVDEC_KV_BF16 = 0, KVDEC_KV_FP8_E4M3 = 1 } kvdec_kv_format;
 
 /* ------------------------------------------------------------------------ */
 /* MHA / GQA / MQA decode                                                   */
@@ -85,6 +93,16 @@ typedef enum kvdec_dtype { KVDEC_F32 = 0, KVDEC_BF16 = 1 } kvdec_dtype;
  *   seqlens int32 [batch]
  *   out    [batch, num_heads, head_dim], F32 or BF16 (out_dtype)
  *   lse    fp32 [batch, num_heads] or NULL
+ * FP8 cache (kv_format = KVDEC_KV_FP8_E4M3, head_dim 128 only): k and v hold
+ *   one E4M3 byte per element in the same layouts; k_scale and v_scale are
+ *   fp32 [num_kv_heads] device arrays (required); K = E4M3(k) * k_scale[kv],
+ *   V = E4M3(v) * v_scale[kv].  q is taken in f16 (|q| < 65504).
+ * Sliding window (window = w > 0, [ARG] §五.3: the query at position t sees
+ *   positions t-w+1 .. t and the cache keeps only those): the cache is a ring
+ *   of w slots, position p in slot p mod w (kvdec_append_rope with the same
+ *   window writes it so); seqlens[b] counts every token of the sequence and
+ *   may exceed the capacity, and the step reads the min(seqlens[b], w) slots.
+ *   w must not exceed the capacity (contiguous) or max_blocks * 64 (paged).
  * Supported: head_dim in {64, 128}; num_heads % num_kv_heads == 0;
  * q, k, v, out 16-byte aligned.  scale == 0 selects 1/sqrt(head_dim); any other
  * scale must be positive and finite (KVDEC_ERR_INVALID_ARG otherwise).
@@ -114,6 +132,10 @@ typedef struct kvdec_gqa_params {
     size_t workspace_bytes;
     uint32_t* error_flag;    /* optional */
     int32_t max_ctas;        /* work items (CTAs); 0 = one wave of resident CTAs */
+    int32_t kv_format;       /* kvdec_kv_format; 0 = bf16 */
+    const float* k_scale;    /* FP8 only: fp32 [num_kv_heads] */
+    const float* v_scale;    /* FP8 only: fp32 [num_kv_heads] */
+    int32_t window;          /* 0 = all seqlens[b] tokens; w > 0 = ring cache of w slots */
     int32_t reserved;
 } kvdec_gqa_params;
 
@@ -218,8 +240,14 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream);
  *   -> K[.., pos, :] = RoPE_pos(k_new) (all head_dim values rotated),
  *      V[.., pos, :] = v_new, contiguous (block_table NULL) or paged layout
  *      exactly as in kvdec_gqa_decode.
- * pos outside [0, capacity) or a bad page entry sets the error bit and the
- * row is skipped.
+ *   window = w > 0 (GQA only): the row goes to ring slot pos mod w (the
+ *   rotation still uses pos), matching kvdec_gqa_decode's sliding window.
+ *   kv_format = KVDEC_KV_FP8_E4M3 (GQA only, head_dim 128): K code =
+ *   E4M3(RoPE_pos(k_new) / k_scale[kv]) from the binary32 rotation, V code =
+ *   E4M3(v_new / v_scale[kv]) from the correctly rounded binary32 quotient;
+ *   nearest-even, magnitudes above 448 saturate to 448.
+ * pos (or its ring slot) outside [0, capacity) or a bad page entry sets the
+ * error bit and the row is skipped.
  */
 typedef enum kvdec_append_mode { KVDEC_APPEND_MLA = 0, KVDEC_APPEND_GQA = 1 } kvdec_append_mode;
 
@@ -245,6 +273,10 @@ typedef struct kvdec_append_params {
     int32_t capacity;            /* GQA contiguous */
     int32_t reserved;
     uint32_t* error_flag;        /* optional */
+    int32_t kv_format;           /* GQA: kvdec_kv_format; 0 = bf16 */
+    int32_t window;              /* GQA: 0, or w > 0 for a ring cache of w slots */
+    const float* k_scale;        /* FP8: fp32 [num_kv_heads] */
+    const float* v_scale;        /* FP8: fp32 [num_kv_heads] */
 } kvdec_append_params;
 
 kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream);

@@ -165,15 +165,18 @@ def gqa_case(B, h, n_kv, d, *, seqlens=None, lo=None, hi=None, cap=None,
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     held = sl.clamp(max=window) if window > 0 else sl      # slots holding data
+    ring_pages = (window + PAGE - 1) // PAGE                 # a ring has >= window slots
     if not paged:
         if cap is None:
             mx = int(held.max().item()) if B > 0 else 0
-            cap = max(PAGE, (mx + PAGE - 1) // PAGE * PAGE)
+            cap = max(PAGE, (mx + PAGE - 1) // PAGE * PAGE, ring_pages * PAGE)
         k = _randn_bf16((B, n_kv, cap, d), g, device)
         v = _randn_bf16((B, n_kv, cap, d), g, device)
         case = GqaCase(q, k, v, sl, None, scale, cap, window=window)
     else:
-        bt, num_pages = shuffled_block_table(held, g, device, spare_pages)
+        need = [(int(x) + PAGE - 1) // PAGE for x in held.to("cpu").tolist()]
+        mb = max(need + [1, ring_pages])
+        bt, num_pages = shuffled_block_table(held, g, device, spare_pages, mb)
         k = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
         v = _randn_bf16((num_pages, n_kv, PAGE, d), g, device)
         cap = bt.shape[1] * PAGE
@@ -248,10 +251,19 @@ CONFIG_INDEX = {"C0": 0, "C1": 1, "C2-MHA": 2, "C2-MQA": 2, "C3": 3,
                 "C4-MLA": 4, "C4-GQA": 4}
 
 
-def config_case(name: str, device="cpu"):
+def config_case(name: str, device="cpu", kv_dtype="bf16"):
     """The named workload with its seed (1000 + config index).  C2-MHA and
-    C2-MQA draw the same q (the seed's first draw) and independent K/V."""
+    C2-MQA draw the same q (the seed's first draw) and independent K/V.
+    ``kv_dtype="fp8"`` (GQA workloads) turns the cache into E4M3 codes."""
     c = CONFIGS[name]
+    if kv_dtype != "bf16":
+        if c["kind"] != "gqa":
+            raise ValueError("an FP8 cache is built for the GQA workloads")
+        case = config_case(name, device)
+        g = _gen(SEED_BASE + 500 + CONFIG_INDEX[name], device)
+        case.k, case.k_scale = fp8_codes(case.k, g, device)
+        case.v, case.v_scale = fp8_codes(case.v, g, device)
+        return case
     seed = SEED_BASE + CONFIG_INDEX[name]
     if c["kind"] == "mla":
         return mla_case(c["B"], c["n_h"], lo=c["lo"], hi=c["hi"], seed=seed,

@@ -33,7 +33,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts(lib):
-    assert lib.kvdec_abi_version() == 1
+    assert lib.kvdec_abi_version() == kvdec.ABI_VERSION == 2
     for kind, st in enumerate([kvdec.GqaParams, kvdec.MlaParams, kvdec.AppendParams,
                                kvdec.CombineParams, kvdec.MlaProjParams]):
         assert lib.kvdec_params_size(kind) == ctypes.sizeof(st)
@@ -86,3 +86,33 @@ def test_projection_argument_checks(lib):
     p.out_dtype, p.x = kvdec.F32, 257
     assert lib.kvdec_mla_absorb_q(ctypes.byref(p), None) == 1
     assert "aligned" in lib.kvdec_last_error().decode()
+
+
+def test_fp8_and_window_argument_checks(lib):
+    """FP8 cache and sliding-window arguments that are rejected on the host
+    before any device query."""
+    p = kvdec.GqaParams()
+    p.batch, p.num_heads, p.num_kv_heads, p.head_dim = 2, 8, 2, 64
+    p.kv_format = kvdec.KV_FP8_E4M3
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 2       # FP8 needs head_dim 128
+    assert "FP8" in lib.kvdec_last_error().decode()
+    p.kv_format = 5
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 1
+    assert "kv_format" in lib.kvdec_last_error().decode()
+    p.kv_format, p.head_dim, p.window = kvdec.KV_BF16, 128, -1
+    assert lib.kvdec_gqa_decode(ctypes.byref(p), None) == 1
+    assert "window" in lib.kvdec_last_error().decode()
+    assert lib.kvdec_gqa_workspace_bytes(ctypes.byref(p)) == 0
+    a = kvdec.AppendParams()
+    a.mode, a.batch, a.seqlens = kvdec.APPEND_MLA, 1, 16
+    a.window = 8
+    assert lib.kvdec_append_rope(ctypes.byref(a), None) == 2      # MLA takes no window
+    a.mode, a.window = kvdec.APPEND_GQA, 0
+    a.k_new, a.v_new, a.k, a.v = 256, 512, 1024, 2048
+    a.num_kv_heads, a.head_dim, a.capacity = 2, 128, 64
+    a.kv_format = kvdec.KV_FP8_E4M3                                # no scales
+    assert lib.kvdec_append_rope(ctypes.byref(a), None) == 1
+    assert "k_scale" in lib.kvdec_last_error().decode()
+    a.kv_format, a.window = kvdec.KV_BF16, 65                      # more than the 64 slots
+    assert lib.kvdec_append_rope(ctypes.byref(a), None) == 1
+    assert "window" in lib.kvdec_last_error().decode()

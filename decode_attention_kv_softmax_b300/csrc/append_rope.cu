@@ -16,6 +16,8 @@
 // (nearest-even, saturating at 448; the quotient is the correctly rounded
 // binary32 one), and a sliding window of w tokens ([ARG] §五.3) writes the
 // ring slot pos mod w while the rotation keeps the position pos.
+#include <cuda_fp8.h>
+
 #include "common.cuh"
 #include "kernels.h"
 

@@ -5,7 +5,6 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -300,12 +299,17 @@ KVDEC_DEVINL uint32_t ld_shared_u32(uint32_t addr) {
     return v;
 }
 
-// Two E4M3 codes (bits 0-7 the first, 8-15 the second) -> f16x2 (first in the
-// low half).  Exact: every E4M3 value, subnormals included, is an f16 number.
-KVDEC_DEVINL uint32_t e4m3x2_to_f16x2(uint32_t codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(codes & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes (byte k = code k) -> two f16x2: lo = (code 0, code 1),
+// hi = (code 2, code 3), the first of each pair in the low half.  The 32-bit
+// register is split into its 16-bit halves in place, one conversion each.
+// Exact: every E4M3 value, subnormals included, is an f16 number.
+KVDEC_DEVINL void e4m3x4_to_f16x2x2(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(codes));
 }
 
 // bf16x2 -> f16x2 (exact for |x| in f16's normal range)

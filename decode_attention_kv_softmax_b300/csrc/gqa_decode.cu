@@ -252,9 +252,11 @@ __global__ void __launch_bounds__(160, 2)
                         uint32_t r[4];
                         ldsm_x4(kb + swz128(tok, chunk), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            mma_f16_16816(s[nt], qa[4 * kk + i], e4m3x2_to_f16x2(r[i]),
-                                          e4m3x2_to_f16x2(r[i] >> 16));
+                        for (int i = 0; i < 4; ++i) {
+                            uint32_t b0, b1;
+                            e4m3x4_to_f16x2x2(r[i], b0, b1);
+                            mma_f16_16816(s[nt], qa[4 * kk + i], b0, b1);
+                        }
                     }
                 } else {
 #pragma unroll
@@ -331,14 +333,16 @@ __global__ void __launch_bounds__(160, 2)
                         const uint32_t w1 = ld_shared_u32(vb + swz128(tk + 1, chunk) + sub);
                         const uint32_t w2 = ld_shared_u32(vb + swz128(tk + 8, chunk) + sub);
                         const uint32_t w3 = ld_shared_u32(vb + swz128(tk + 9, chunk) + sub);
-                        // byte pairs per dim: lo word (dims 0, 1), hi word (dims 2, 3)
-                        const uint32_t p01[2] = {__byte_perm(w0, w1, 0x5140), __byte_perm(w0, w1, 0x7362)};
-                        const uint32_t p23[2] = {__byte_perm(w2, w3, 0x5140), __byte_perm(w2, w3, 0x7362)};
+                        // byte pairs per dim (dims 0, 1 | dims 2, 3), widened:
+                        // bl[i] = tokens (tk, tk+1) of dim i, bh[i] = (tk+8, tk+9)
+                        uint32_t bl[4], bh[4];
+                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x5140), bl[0], bl[1]);
+                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x7362), bl[2], bl[3]);
+                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x5140), bh[0], bh[1]);
+                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x7362), bh[2], bh[3]);
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const int sh = 16 * (i & 1);
-                            uint32_t b0 = e4m3x2_to_f16x2(p01[i >> 1] >> sh);
-                            uint32_t b1 = e4m3x2_to_f16x2(p23[i >> 1] >> sh);
+                            uint32_t b0 = bl[i], b1 = bh[i];
                             if (partial) {
                                 b0 &= keep_lo;
                                 b1 &= keep_hi;

@@ -165,11 +165,12 @@ __global__ void __launch_bounds__(160, 2)
     const int mt_w = warp / WPM;
     const int tok_base = (warp % WPM) * TPW;
 
-    // units with no tokens: out = 0, lse = -inf (shared out round-robin)
-    for (int b = 0; b < a.B; ++b) {
+    // units with no tokens: out = 0, lse = -inf (unit u is handled by item
+    // u mod W: step through this item's units only)
+    for (int u = w; u < a.B * S.upb; u += S.W) {
+        const int b = u / S.upb, j = u % S.upb;
         if (S.ntiles(b) != 0) continue;
-        for (int j = 0; j < S.upb; ++j) {
-            if ((b * S.upb + j) % S.W != w) continue;
+        {
             const int kvh = j / a.n_hc, hc = j % a.n_hc;
             const int nr = min(a.hc_rows, a.g - hc * a.hc_rows);
             for (int i = tid; i < nr * D; i += 128) {

@@ -291,8 +291,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         uint32_t hand_waits[2] = {0u, 0u};
 
         // sequences with no tokens
-        for (int b = 0; b < a.B; ++b) {
-            if (w >= S.W || S.ntiles(b) != 0 || b % S.W != w) continue;
+        // (sequence b is this pair's when b mod W = w: step through those only)
+        for (int b = w; w < S.W && b < a.B; b += S.W) {
+            if (S.ntiles(b) != 0) continue;
             const size_t base = ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * g;
             for (int c = 0; c < 128; c += 4) {
                 if (a.out_bf16)

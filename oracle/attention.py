@@ -288,6 +288,47 @@ def mla_decode_nonabsorbed(q_nope, q_rope, cache, block_table, seqlens,
     return out, lse
 
 
+def mla_prefill_expand(c_kv, W_UK, W_UV):
+    """The up-projection of a prefill chunk ([ARG] §四.6: one ordinary
+    weight GEMM over all s tokens; [MLA] §4.2.1: prefill computes k and v
+    explicitly): K^C[t, h, :] = W_UK,h c_kv_t and V[t, h, :] = W_UV,h c_kv_t
+    for c_kv [s, 512] and W_UK, W_UV [n_h, 128, 512].  Returns both
+    [s, n_h, 128]."""
+    c = np.asarray(c_kv, dtype=np.float64)
+    return (np.einsum("tc,hdc->thd", c, np.asarray(W_UK, dtype=np.float64)),
+            np.einsum("tc,hdc->thd", c, np.asarray(W_UV, dtype=np.float64)))
+
+
+def mla_prefill(q_nope, q_rope, k_nope, k_rope, v, scale=None, kv_offset=None):
+    """Causal MLA attention of a prefill chunk on the non-absorbed path
+    ([ARG] §四.6: after the up-projection, standard causal attention with
+    head dims 192 (q.k) and 128 (v); §五.3 causal mask).
+
+    q_nope [s_q, n_h, 128], q_rope [s_q, n_h, 64] (rotated); k_nope
+    [s_kv, n_h, 128], k_rope [s_kv, 64] (rotated, shared by every head),
+    v [s_kv, n_h, 128].  Query i sits at position kv_offset + i (default
+    s_kv - s_q: the chunk is the newest s_q tokens) and sees keys
+    j <= kv_offset + i.  scale defaults to 1/sqrt(192).  Returns out
+    [s_q, n_h, 128] and lse [s_q, n_h]."""
+    s_q, n_h, dn = q_nope.shape
+    s_kv = k_nope.shape[0]
+    if kv_offset is None:
+        kv_offset = s_kv - s_q
+    if scale is None:
+        scale = 1.0 / math.sqrt(dn + q_rope.shape[2])
+    out = np.zeros((s_q, n_h, v.shape[2]))
+    lse = np.zeros((s_q, n_h))
+    for hh in range(n_h):
+        K = np.concatenate([k_nope[:, hh], k_rope], axis=1)       # [s_kv, 192]
+        for i in range(s_q):
+            L = min(s_kv, kv_offset + i + 1)
+            q = np.concatenate([q_nope[i, hh], q_rope[i, hh]])[None]
+            o, l = attend(q, K[:L], v[:L, hh], scale)
+            out[i, hh] = o[0]
+            lse[i, hh] = l[0]
+    return out, lse
+
+
 # ----------------------------------------------------------------------------
 # flash-decoding split and merge ([ARG] §五.2, last paragraph: split the KV
 # along the sequence, softmax each piece locally, then merge the normalisers)

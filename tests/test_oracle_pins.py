@@ -354,6 +354,76 @@ def test_append_gqa_contiguous_and_paged():
     np.testing.assert_array_equal(Vp2[2, :, 3], vn[1])
 
 
+# ---------------------------------------------------------------- MLA prefill (non-absorbed)
+
+def _prefill_case(s_kv, s_q, n_h, seed):
+    r = np.random.default_rng(seed)
+    c_kv = r.normal(size=(s_kv, 512))
+    k_rope = r.normal(size=(s_kv, 64))
+    q_nope = r.normal(size=(s_q, n_h, 128)) / 4
+    q_rope = r.normal(size=(s_q, n_h, 64)) / 4
+    W_UK = r.normal(size=(n_h, 128, 512)) / math.sqrt(512)
+    W_UV = r.normal(size=(n_h, 128, 512)) / math.sqrt(512)
+    return c_kv, k_rope, q_nope, q_rope, W_UK, W_UV
+
+
+def test_mla_prefill_rows_equal_absorbed_path():
+    """Every query row of the non-absorbed causal prefill equals the absorbed
+    decode over that row's prefix ([ARG] §四.5-6: the two paths are the same
+    attention; the pinned absorbed functions serve as the check)."""
+    s_kv, s_q, n_h = 70, 6, 2
+    c_kv, k_rope, q_nope, q_rope, W_UK, W_UV = _prefill_case(s_kv, s_q, n_h, 31)
+    k_nope, v = oracle.mla_prefill_expand(c_kv, W_UK, W_UV)
+    out, lse = oracle.mla_prefill(q_nope, q_rope, k_nope, k_rope, v)
+    cache = np.zeros((2, 64, 576))
+    rows = np.concatenate([c_kv, k_rope], axis=1)
+    cache.reshape(128, 576)[:s_kv] = rows
+    bt = np.array([[0, 1]] * s_q)
+    sl = np.array([s_kv - s_q + i + 1 for i in range(s_q)])
+    q_abs = oracle.mla_absorb_q(q_nope, W_UK)
+    lat, lse_a = oracle.mla_decode_absorbed(q_abs, q_rope, cache, bt, sl)
+    np.testing.assert_allclose(out, oracle.mla_project_out(lat, W_UV), atol=1e-11)
+    np.testing.assert_allclose(lse, lse_a, atol=1e-11)
+    # a chunk placed at another offset is a different (wrong) causal window
+    wrong, _ = oracle.mla_prefill(q_nope, q_rope, k_nope, k_rope, v, kv_offset=s_kv - s_q - 3)
+    assert not np.allclose(wrong, out, atol=1e-6)
+
+
+def test_mla_prefill_is_causal():
+    """Query i sees positions <= s_kv - s_q + i and nothing after them."""
+    s_kv, s_q, n_h = 40, 8, 1
+    c_kv, k_rope, q_nope, q_rope, W_UK, W_UV = _prefill_case(s_kv, s_q, n_h, 32)
+    k_nope, v = oracle.mla_prefill_expand(c_kv, W_UK, W_UV)
+    out, _ = oracle.mla_prefill(q_nope, q_rope, k_nope, k_rope, v)
+    i = 3
+    last = s_kv - s_q + i
+    k2, v2, r2 = k_nope.copy(), v.copy(), k_rope.copy()
+    k2[last + 1:] += 5.0
+    v2[last + 1:] -= 7.0
+    r2[last + 1:] *= -1
+    out2, _ = oracle.mla_prefill(q_nope, q_rope, k2, r2, v2)
+    np.testing.assert_array_equal(out2[: i + 1], out[: i + 1])
+    assert not np.allclose(out2[i + 1:], out[i + 1:])
+    v3 = v.copy()
+    v3[last] += 1.0
+    out3, _ = oracle.mla_prefill(q_nope, q_rope, k_nope, k_rope, v3)
+    assert not np.allclose(out3[i], out[i])
+
+
+def test_mla_prefill_single_query_is_decode():
+    """A one-token chunk is a decode step on the literal path."""
+    s_kv, n_h = 65, 3
+    c_kv, k_rope, q_nope, q_rope, W_UK, W_UV = _prefill_case(s_kv, 1, n_h, 33)
+    k_nope, v = oracle.mla_prefill_expand(c_kv, W_UK, W_UV)
+    out, lse = oracle.mla_prefill(q_nope, q_rope, k_nope, k_rope, v)
+    cache = np.zeros((2, 64, 576))
+    cache.reshape(128, 576)[:s_kv] = np.concatenate([c_kv, k_rope], axis=1)
+    ref, lref = oracle.mla_decode_nonabsorbed(q_nope, q_rope, cache, np.array([[0, 1]]),
+                                              np.array([s_kv]), W_UK, W_UV)
+    np.testing.assert_allclose(out, ref, atol=1e-12)
+    np.testing.assert_allclose(lse, lref, atol=1e-12)
+
+
 # ---------------------------------------------------------------- E4M3 (FP8 KV cache)
 
 def test_e4m3_decode_golden():

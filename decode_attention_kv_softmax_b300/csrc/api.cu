@@ -228,6 +228,8 @@ int64_t kvdec_params_size(int kind) {
         case 2: return (int64_t)sizeof(kvdec_append_params);
         case 3: return (int64_t)sizeof(kvdec_combine_params);
         case 4: return (int64_t)sizeof(kvdec_mla_proj_params);
+        case 5: return (int64_t)sizeof(kvdec_mla_expand_params);
+        case 6: return (int64_t)sizeof(kvdec_mla_prefill_params);
         default: return -1;
     }
 }
@@ -429,6 +431,7 @@ static kvdec_status mla_proj(const kvdec_mla_proj_params* p, void* stream, bool 
     a.batch = p->batch;
     a.num_heads = p->num_heads;
     a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    a.x_shared = 0;
     cudaError_t e = kvdec::launch_mla_proj(absorb, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, name);
     return KVDEC_OK;
@@ -438,6 +441,70 @@ kvdec_status kvdec_mla_absorb_q(const kvdec_mla_proj_params* p, void* stream) { 
 
 kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream) {
     return mla_proj(p, stream, false);
+}
+
+kvdec_status kvdec_mla_prefill_expand(const kvdec_mla_expand_params* p, void* stream) {
+    const char* name = "kvdec_mla_prefill_expand";
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "%s: params is NULL", name);
+    if (!p->c_kv || !p->w_uk || !p->w_uv || !p->k_nope || !p->v)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: c_kv, w_uk, w_uv, k_nope and v must be non-NULL", name);
+    if (!aligned(p->c_kv, 16) || !aligned(p->w_uk, 16) || !aligned(p->w_uv, 16) || !aligned(p->k_nope, 16) ||
+        !aligned(p->v, 16))
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
+    if (p->s < 1 || p->s > (1 << 20) || p->num_heads < 1 || p->num_heads > 65535)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: s %d, num_heads %d", name, p->s, p->num_heads);
+    kvdec::MlaProjArgs a;
+    a.x = static_cast<const __nv_bfloat16*>(p->c_kv);
+    a.batch = p->s;
+    a.num_heads = p->num_heads;
+    a.out_bf16 = 1;
+    a.x_shared = 1;
+    a.w = static_cast<const __nv_bfloat16*>(p->w_uk);
+    a.y = p->k_nope;
+    cudaError_t e = kvdec::launch_mla_proj(false, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    a.w = static_cast<const __nv_bfloat16*>(p->w_uv);
+    a.y = p->v;
+    e = kvdec::launch_mla_proj(false, a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return KVDEC_OK;
+}
+
+kvdec_status kvdec_mla_prefill(const kvdec_mla_prefill_params* p, void* stream) {
+    const char* name = "kvdec_mla_prefill";
+    if (!p) return fail(KVDEC_ERR_INVALID_ARG, "%s: params is NULL", name);
+    if (!p->q_nope || !p->q_rope || !p->k_nope || !p->k_rope || !p->v || !p->out)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: q_nope, q_rope, k_nope, k_rope, v and out must be non-NULL", name);
+    if (!aligned(p->q_nope, 16) || !aligned(p->q_rope, 16) || !aligned(p->k_nope, 16) || !aligned(p->k_rope, 16) ||
+        !aligned(p->v, 16) || !aligned(p->out, 16) || (p->lse && !aligned(p->lse, 4)))
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
+    if (p->s_q < 1 || p->s_kv < 1 || p->s_kv > (1 << 24) || p->num_heads < 1 || p->num_heads > 65535)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: s_q %d, s_kv %d, num_heads %d", name, p->s_q, p->s_kv, p->num_heads);
+    const int off = p->kv_offset < 0 ? p->s_kv - p->s_q : p->kv_offset;
+    if (off < 0 || (int64_t)off + p->s_q > p->s_kv)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: queries at positions %d..%d need s_kv %d >= that", name, off,
+                    off + p->s_q - 1, p->s_kv);
+    if (p->out_dtype != KVDEC_F32 && p->out_dtype != KVDEC_BF16)
+        return fail(KVDEC_ERR_INVALID_ARG, "%s: out_dtype %d", name, p->out_dtype);
+    if (!scale_ok(p->scale)) return fail(KVDEC_ERR_INVALID_ARG, "%s: scale %g", name, (double)p->scale);
+    kvdec::MlaPrefillArgs a;
+    a.q_nope = static_cast<const __nv_bfloat16*>(p->q_nope);
+    a.q_rope = static_cast<const __nv_bfloat16*>(p->q_rope);
+    a.k_nope = static_cast<const __nv_bfloat16*>(p->k_nope);
+    a.k_rope = static_cast<const __nv_bfloat16*>(p->k_rope);
+    a.v = static_cast<const __nv_bfloat16*>(p->v);
+    a.out = p->out;
+    a.lse = p->lse;
+    a.s_q = p->s_q;
+    a.s_kv = p->s_kv;
+    a.num_heads = p->num_heads;
+    a.kv_offset = off;
+    a.out_bf16 = p->out_dtype == KVDEC_BF16;
+    const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
+    a.scale_log2 = (float)(scale * 1.4426950408889634);
+    cudaError_t e = kvdec::launch_mla_prefill(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, name);
+    return KVDEC_OK;
 }
 
 kvdec_status kvdec_combine_splits(const kvdec_combine_params* p, void* stream) {

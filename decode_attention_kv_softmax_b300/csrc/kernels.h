@@ -95,10 +95,25 @@ struct MlaProjArgs {
     const __nv_bfloat16* w;   // [H, 128, 512]
     void* y;                  // absorb: [B, H, 512]; project: [B, H, 128]
     int batch, num_heads, out_bf16;
+    int x_shared;             // x is one [B, K] matrix for every head (prefill up-projection)
 };
 
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st);
 cudaError_t launch_mla_proj(bool absorb, const MlaProjArgs& a, cudaStream_t st);
+
+// Causal MLA prefill attention on the non-absorbed path (mla_prefill.cu)
+struct MlaPrefillArgs {
+    const __nv_bfloat16* q_nope;   // [s_q, H, 128]
+    const __nv_bfloat16* q_rope;   // [s_q, H, 64]
+    const __nv_bfloat16* k_nope;   // [s_kv, H, 128]
+    const __nv_bfloat16* k_rope;   // [s_kv, 64]
+    const __nv_bfloat16* v;        // [s_kv, H, 128]
+    void* out;                     // [s_q, H, 128]
+    float* lse;                    // [s_q, H] or null
+    int s_q, s_kv, num_heads, kv_offset, out_bf16;
+    float scale_log2;
+};
+cudaError_t launch_mla_prefill(const MlaPrefillArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -3,7 +3,9 @@
 // §4), per sequence b and head h:
 //   absorb:  q~[b,h,:]  = W_UK[h]^T q^C[b,h,:]   (128 -> 512)
 //   project: o[b,h,:]   = W_UV[h]   o~[b,h,:]    (512 -> 128)
-// with W_UK, W_UV [n_h, 128, 512] bf16.  For every head this is a small
+// with W_UK, W_UV [n_h, 128, 512] bf16.  With x_shared the input rows are
+// one [batch, K] matrix for every head: the prefill up-projection
+// K^C[t, h] = W_UK[h] c_kv[t], V[t, h] = W_UV[h] c_kv[t] ([ARG] §四.6).  For every head this is a small
 // GEMM over the batch: Y_h[B x N] = X_h[B x K] . W_h (absorb: K = 128,
 // N = 512, W_h stored [K][N]) or X_h . W_h^T (project: K = 512, N = 128, W_h
 // stored [N][K]).  At decode batch sizes it reads the 16.8 MB of weights
@@ -68,7 +70,8 @@ __global__ void __launch_bounds__(128) mla_proj_kernel(const MlaProjArgs a) {
         for (int i = tid; i < kM * 8; i += 128) {
             const int r = i >> 3, c = i & 7;
             const bool ok = m0 + r < a.batch;
-            const __nv_bfloat16* src = X + ((size_t)(ok ? m0 + r : 0) * a.num_heads + h) * K + kc * kKC + c * 8;
+            const size_t xr = (size_t)(ok ? m0 + r : 0);
+            const __nv_bfloat16* src = X + (a.x_shared ? xr : xr * a.num_heads + h) * K + kc * kKC + c * 8;
             cp_async16(sa + swz128(r, c), src, ok);
         }
         if (ABSORB) {

@@ -70,11 +70,24 @@ class MlaProjParams(ctypes.Structure):
                 ("num_heads", c_int32), ("out_dtype", c_int32), ("reserved", c_int32)]
 
 
+class MlaExpandParams(ctypes.Structure):
+    _fields_ = [("c_kv", c_void_p), ("w_uk", c_void_p), ("w_uv", c_void_p), ("k_nope", c_void_p),
+                ("v", c_void_p), ("s", c_int32), ("num_heads", c_int32)]
+
+
+class MlaPrefillParams(ctypes.Structure):
+    _fields_ = [("q_nope", c_void_p), ("q_rope", c_void_p), ("k_nope", c_void_p),
+                ("k_rope", c_void_p), ("v", c_void_p), ("s_q", c_int32), ("s_kv", c_int32),
+                ("num_heads", c_int32), ("kv_offset", c_int32), ("scale", c_float),
+                ("out_dtype", c_int32), ("out", c_void_p), ("lse", c_void_p)]
+
+
 EXPORTS = ["kvdec_abi_version", "kvdec_params_size", "kvdec_status_string",
            "kvdec_last_error", "kvdec_gqa_workspace_bytes", "kvdec_gqa_decode",
            "kvdec_mla_workspace_bytes", "kvdec_mla_decode_absorbed", "kvdec_append_rope",
            "kvdec_combine_splits", "kvdec_selftest_wait_timeout",
-           "kvdec_gqa_decode_noalloc", "kvdec_mla_absorb_q", "kvdec_mla_project_out"]
+           "kvdec_gqa_decode_noalloc", "kvdec_mla_absorb_q", "kvdec_mla_project_out",
+           "kvdec_mla_prefill_expand", "kvdec_mla_prefill"]
 
 _lib = None
 _lock = threading.Lock()
@@ -106,7 +119,9 @@ def load(path: str = LIB_PATH):
                          ("kvdec_append_rope", AppendParams),
                          ("kvdec_combine_splits", CombineParams),
                          ("kvdec_mla_absorb_q", MlaProjParams),
-                         ("kvdec_mla_project_out", MlaProjParams)]:
+                         ("kvdec_mla_project_out", MlaProjParams),
+                         ("kvdec_mla_prefill_expand", MlaExpandParams),
+                         ("kvdec_mla_prefill", MlaPrefillParams)]:
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(st), c_void_p]
@@ -114,7 +129,8 @@ def load(path: str = LIB_PATH):
         lib.kvdec_selftest_wait_timeout.argtypes = [c_uint64, c_void_p, c_void_p]
         if lib.kvdec_abi_version() != ABI_VERSION:
             raise RuntimeError("libkvdec ABI version mismatch")
-        for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams, MlaProjParams]):
+        for kind, st in enumerate([GqaParams, MlaParams, AppendParams, CombineParams, MlaProjParams,
+                                   MlaExpandParams, MlaPrefillParams]):
             if lib.kvdec_params_size(kind) != ctypes.sizeof(st):
                 raise RuntimeError(f"params struct {st.__name__} layout mismatch")
         _lib = lib
@@ -490,3 +506,48 @@ def selftest_wait_timeout(timeout_ns: int, error_flag, stream=None):
 
 def default_scale_gqa(d: int) -> float:
     return 1.0 / math.sqrt(d)
+
+
+# ---------------------------------------------------------------- MLA prefill (non-absorbed)
+
+def mla_prefill_expand(c_kv, W_UK, W_UV, stream=None):
+    """kvdec_mla_prefill_expand: k_nope[t,h] = W_UK[h] c_kv[t], v[t,h] =
+    W_UV[h] c_kv[t].  c_kv [s, 512] bf16; W_UK, W_UV [n_h, 128, 512] bf16.
+    Returns (k_nope, v), bf16 [s, n_h, 128]."""
+    lib = load()
+    dev = c_kv.device
+    for t, n in [(c_kv, "c_kv"), (W_UK, "W_UK"), (W_UV, "W_UV")]:
+        _need(t, n, torch.bfloat16, dev)
+    s_len, n_h = c_kv.shape[0], W_UK.shape[0]
+    k_nope = torch.empty((s_len, n_h, 128), dtype=torch.bfloat16, device=dev)
+    v = torch.empty_like(k_nope)
+    p = MlaExpandParams()
+    p.c_kv, p.w_uk, p.w_uv, p.k_nope, p.v = _ptr(c_kv), _ptr(W_UK), _ptr(W_UV), _ptr(k_nope), _ptr(v)
+    p.s, p.num_heads = s_len, n_h
+    _check(lib.kvdec_mla_prefill_expand(ctypes.byref(p), _stream(stream)), "kvdec_mla_prefill_expand")
+    return k_nope, v
+
+
+def mla_prefill(q_nope, q_rope, k_nope, k_rope, v, kv_offset=-1, scale=None,
+                out_dtype=torch.float32, return_lse=True, stream=None):
+    """kvdec_mla_prefill: causal attention of a prefill chunk on the
+    non-absorbed path.  q_nope [s_q, n_h, 128], q_rope [s_q, n_h, 64],
+    k_nope, v [s_kv, n_h, 128], k_rope [s_kv, 64], all bf16; query i sits at
+    position kv_offset + i (kv_offset < 0: s_kv - s_q).  Returns (out
+    [s_q, n_h, 128], lse [s_q, n_h] or None)."""
+    lib = load()
+    dev = q_nope.device
+    for t, n in [(q_nope, "q_nope"), (q_rope, "q_rope"), (k_nope, "k_nope"), (k_rope, "k_rope"), (v, "v")]:
+        _need(t, n, torch.bfloat16, dev)
+    s_q, n_h, _ = q_nope.shape
+    out = torch.empty((s_q, n_h, 128), dtype=out_dtype, device=dev)
+    lse = torch.empty((s_q, n_h), dtype=torch.float32, device=dev) if return_lse else None
+    p = MlaPrefillParams()
+    p.q_nope, p.q_rope, p.k_nope, p.k_rope, p.v = (_ptr(q_nope), _ptr(q_rope), _ptr(k_nope),
+                                                    _ptr(k_rope), _ptr(v))
+    p.s_q, p.s_kv, p.num_heads, p.kv_offset = s_q, k_nope.shape[0], n_h, int(kv_offset)
+    p.scale = float(scale) if scale else 0.0
+    p.out_dtype = _dtype_code(out.dtype)
+    p.out, p.lse = _ptr(out), _ptr(lse)
+    _check(lib.kvdec_mla_prefill(ctypes.byref(p), _stream(stream)), "kvdec_mla_prefill")
+    return out, lse

@@ -319,6 +319,68 @@ kvdec_status kvdec_mla_absorb_q(const kvdec_mla_proj_params* p, void* stream);
 kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* MLA prefill on the non-absorbed path                                      */
+/* ------------------------------------------------------------------------ */
+/*
+ * A prefill (or chunked-prefill) step of MLA attention does not absorb:
+ * it up-projects the chunk's latents with one weight GEMM and runs ordinary
+ * causal attention with head dims 192 (q.k) and 128 (v) ([ARG]
+ * "attention-variants-and-kv-cache" §四.6: absorbing would cost ~3.4x the
+ * FLOPs of the s^2 term, which dominates a compute-bound prefill; [MLA]
+ * "multi-head-latent-attention" §4.2.1; causal mask [ARG] §五.3).
+ *
+ * kvdec_mla_prefill_expand: for every token t and head h
+ *   k_nope[t, h, :] = W_UK[h] c_kv[t, :],   v[t, h, :] = W_UV[h] c_kv[t, :]
+ *   c_kv bf16 [s, 512]; W_UK, W_UV bf16 [num_heads, 128, 512] (as for
+ *   kvdec_mla_absorb_q / kvdec_mla_project_out); k_nope, v bf16
+ *   [s, num_heads, 128] (fp32 accumulation, one rounding to bf16).
+ *
+ * kvdec_mla_prefill: for every query i (position kv_offset + i) and head h
+ *   s_j = scale [q_nope ; q_rope][i, h] . [k_nope[j, h] ; k_rope[j]],
+ *         j <= kv_offset + i
+ *   out[i, h, :] = sum_j softmax(s)_j v[j, h, :],  lse[i, h] = ln sum_j e^{s_j}
+ *   q_nope bf16 [s_q, num_heads, 128], q_rope bf16 [s_q, num_heads, 64]
+ *   (rotated); k_nope, v bf16 [s_kv, num_heads, 128]; k_rope bf16 [s_kv, 64]
+ *   (rotated, shared by every head: the second half of the latent cache
+ *   row); out [s_q, num_heads, 128] F32 or BF16; lse fp32 [s_q, num_heads]
+ *   or NULL.  kv_offset < 0 selects s_kv - s_q (the chunk is the newest
+ *   tokens); 0 <= kv_offset and kv_offset + s_q <= s_kv are required.
+ *   scale == 0 selects 1/sqrt(192); otherwise positive and finite.
+ * Ownership: the caller owns every buffer; nothing is allocated; both calls
+ * are asynchronous on `stream`.  Errors: KVDEC_ERR_INVALID_ARG for NULL or
+ * misaligned (16 B) pointers, sizes out of range or another out_dtype.
+ */
+typedef struct kvdec_mla_expand_params {
+    const void* c_kv;
+    const void* w_uk;
+    const void* w_uv;
+    void* k_nope;
+    void* v;
+    int32_t s;
+    int32_t num_heads;
+} kvdec_mla_expand_params;
+
+kvdec_status kvdec_mla_prefill_expand(const kvdec_mla_expand_params* p, void* stream);
+
+typedef struct kvdec_mla_prefill_params {
+    const void* q_nope;
+    const void* q_rope;
+    const void* k_nope;
+    const void* k_rope;
+    const void* v;
+    int32_t s_q;
+    int32_t s_kv;
+    int32_t num_heads;
+    int32_t kv_offset;   /* < 0: s_kv - s_q */
+    float scale;         /* 0 selects 1/sqrt(192) */
+    int32_t out_dtype;
+    void* out;
+    float* lse;          /* optional */
+} kvdec_mla_prefill_params;
+
+kvdec_status kvdec_mla_prefill(const kvdec_mla_prefill_params* p, void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Split combine                                                             */
 /* ------------------------------------------------------------------------ */
 /*
@@ -358,7 +420,8 @@ kvdec_status kvdec_combine_splits(const kvdec_combine_params* p, void* stream);
 /* ------------------------------------------------------------------------ */
 int kvdec_abi_version(void);
 /* sizeof() of each params struct, so a binding can check its mirror:
- * kind 0 gqa, 1 mla, 2 append, 3 combine; -1 for an unknown kind. */
+ * kind 0 gqa, 1 mla, 2 append, 3 combine, 4 mla_proj, 5 mla_expand,
+ * 6 mla_prefill; -1 for an unknown kind. */
 int64_t kvdec_params_size(int kind);
 const char* kvdec_status_string(kvdec_status s);
 const char* kvdec_last_error(void);

@@ -233,6 +233,24 @@ def mla_proj_case(B, n_h=128, *, seed=SEED_BASE, device="cpu"):
     return q_nope, W_UK, W_UV
 
 
+def mla_prefill_case(s_kv, s_q, n_h=128, *, seed=SEED_BASE, device="cpu"):
+    """Inputs of a non-absorbed MLA prefill chunk: c_kv [s_kv, 512] and the
+    rotated rope key k_rope [s_kv, 64] ~ N(0, 1) (a rotation keeps N(0,1),
+    see the module docstring), W_UK, W_UV [n_h, 128, 512] ~ N(0, 1/512) so
+    that the up-projected keys and values are ~N(0, 1), and the chunk's
+    queries q_nope [s_q, n_h, 128], q_rope [s_q, n_h, 64] ~ N(0, 1); all
+    bf16.  Returns a dict."""
+    g = _gen(seed, device)
+    return {
+        "c_kv": _randn_bf16((s_kv, D_C), g, device),
+        "k_rope": _randn_bf16((s_kv, D_R), g, device),
+        "W_UK": _randn_bf16((n_h, 128, D_C), g, device, std=1.0 / math.sqrt(D_C)),
+        "W_UV": _randn_bf16((n_h, 128, D_C), g, device, std=1.0 / math.sqrt(D_C)),
+        "q_nope": _randn_bf16((s_q, n_h, 128), g, device),
+        "q_rope": _randn_bf16((s_q, n_h, D_R), g, device),
+    }
+
+
 # ----------------------------------------------------------------------------
 # the five named workloads
 # ----------------------------------------------------------------------------

@@ -35,7 +35,8 @@ def test_exports_every_declared_symbol(lib):
 def test_struct_layouts(lib):
     assert lib.kvdec_abi_version() == kvdec.ABI_VERSION == 2
     for kind, st in enumerate([kvdec.GqaParams, kvdec.MlaParams, kvdec.AppendParams,
-                               kvdec.CombineParams, kvdec.MlaProjParams]):
+                               kvdec.CombineParams, kvdec.MlaProjParams, kvdec.MlaExpandParams,
+                               kvdec.MlaPrefillParams]):
         assert lib.kvdec_params_size(kind) == ctypes.sizeof(st)
     assert lib.kvdec_params_size(99) == -1
 
@@ -116,3 +117,26 @@ def test_fp8_and_window_argument_checks(lib):
     a.kv_format, a.window = kvdec.KV_BF16, 65                      # more than the 64 slots
     assert lib.kvdec_append_rope(ctypes.byref(a), None) == 1
     assert "window" in lib.kvdec_last_error().decode()
+
+
+def test_prefill_argument_checks(lib):
+    """The prefill entry points reject bad arguments before any launch."""
+    assert lib.kvdec_mla_prefill(None, None) == 1
+    assert lib.kvdec_mla_prefill_expand(None, None) == 1
+    p = kvdec.MlaPrefillParams()
+    p.q_nope, p.q_rope, p.k_nope, p.k_rope, p.v, p.out = 256, 512, 768, 1024, 1280, 1536
+    p.s_q, p.s_kv, p.num_heads, p.kv_offset = 8, 4, 128, -1      # chunk longer than the keys
+    assert lib.kvdec_mla_prefill(ctypes.byref(p), None) == 1
+    assert "s_kv" in lib.kvdec_last_error().decode()
+    p.s_kv, p.kv_offset = 16, 9                                   # 9 + 8 > 16
+    assert lib.kvdec_mla_prefill(ctypes.byref(p), None) == 1
+    p.kv_offset, p.out_dtype = 8, 7
+    assert lib.kvdec_mla_prefill(ctypes.byref(p), None) == 1
+    p.out_dtype, p.scale = kvdec.F32, -1.0
+    assert lib.kvdec_mla_prefill(ctypes.byref(p), None) == 1
+    p.scale, p.k_rope = 0.0, 1025                                 # misaligned
+    assert lib.kvdec_mla_prefill(ctypes.byref(p), None) == 1
+    e = kvdec.MlaExpandParams()
+    e.c_kv, e.w_uk, e.w_uv, e.k_nope, e.v = 256, 512, 768, 1024, 1280
+    e.s, e.num_heads = 0, 128
+    assert lib.kvdec_mla_prefill_expand(ctypes.byref(e), None) == 1

@@ -45,7 +45,9 @@ WORKLOADS = {
     "C3": "DeepSeek-V3-shaped MLA absorbed decode B=64 n_h=128 seqlens U[512,4096] paged latent [pages,64,576]",
     "C4-MLA": "long ragged MLA absorbed decode B=8 n_h=128 seqlens U[16384,131072] paged",
     "C4-GQA": "long ragged Llama-3-70B-shaped GQA decode B=8 h=64 n_kv=8 d=128 seqlens U[16384,131072] paged",
+    "P-MLA": "DeepSeek-V3-shaped MLA prefill chunk, non-absorbed: 4096 tokens, 128 heads, causal (expand + attention)",
 }
+PREFILL_TOKENS = 4096
 
 
 def parse():
@@ -329,8 +331,131 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- main arm
 
+def prefill_flops(s, n_h=128):
+    """Up-projection 2 s 512 (2 x 128 n_h) and causal attention
+    n_h 2 (192 + 128) s^2 / 2 ([ARG] §四.6)."""
+    return 2.0 * s * 512 * 256 * n_h, n_h * 2.0 * 320 * s * s / 2
+
+
+def oracle_prefill_sample(case_cpu, n_rows):
+    """fp64 oracle on the last n_rows queries of the chunk (all heads), the
+    expensive end of the causal triangle; returns (seconds, FLOPs done)."""
+    import oracle
+    s = case_cpu["c_kv"].shape[0]
+    to = lambda t: oracle.bf16_to_f64(t)
+    t0 = time.perf_counter()
+    kn, vv = oracle.mla_prefill_expand(to(case_cpu["c_kv"]), to(case_cpu["W_UK"]), to(case_cpu["W_UV"]))
+    oracle.mla_prefill(to(case_cpu["q_nope"][-n_rows:]), to(case_cpu["q_rope"][-n_rows:]), kn,
+                       to(case_cpu["k_rope"]), vv, kv_offset=s - n_rows)
+    dt = time.perf_counter() - t0
+    fe, _ = prefill_flops(s)
+    return dt, fe + 128 * 2.0 * 320 * s * n_rows
+
+
+def bench_prefill(args, reference=False):
+    """--config P-MLA: one step = kvdec_mla_prefill_expand + kvdec_mla_prefill
+    on a 4096-token chunk; value in TFLOP/s of algorithmic FLOPs."""
+    import torch
+    import kvgen
+    s = PREFILL_TOKENS
+    fe, fa = prefill_flops(s)
+    if reference:
+        case = kvgen.mla_prefill_case(s, s, 128, seed=1005, device="cpu")
+        n = 1
+        dt, fl = oracle_prefill_sample(case, n)
+        times = [oracle_prefill_sample(case, n)[0] for _ in range(max(1, min(args.steps, 3)))]
+        v = fl / (sum(times) / len(times)) / 1e12
+        line = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "impl": "reference", "n_gpus": 1,
+                "steps": len(times), "warmup": 0, "ms_per_step": sum(times) / len(times) * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": WORKLOADS["P-MLA"], "sample_rows": n},
+                "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+                                 "sample": f"up-projection of all {s} tokens + the last {n} query row(s)"},
+                "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    from decode_attention_kv_softmax_b300 import kvdec
+    kvdec.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    stream = torch.cuda.current_stream()
+    hbm_peak, bf16_peak, bf16_sust, peak_src = measured_peaks()
+    c = kvgen.mla_prefill_case(s, s, 128, seed=1005, device=dev)
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        k, v = kvdec.mla_prefill_expand(c["c_kv"], c["W_UK"], c["W_UV"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        out, lse = kvdec.mla_prefill(c["q_nope"], c["q_rope"], k, c["k_rope"], v, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        return out
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(0)
+    clk.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    exp_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    att_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    value = (fe + fa) / (ms * 1e-3) / 1e12
+    att_tf = fa / (att_ms * 1e-3) / 1e12
+    # end to end: the chunk's inputs from pinned host memory, the output back
+    host = {k: t.detach().to("cpu").pin_memory() for k, t in c.items()}
+    hout = torch.empty((s, 128, 128), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    n_e2e = 3
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n_e2e):
+        for k, t in host.items():
+            c[k].copy_(t, non_blocking=True)
+        hout.copy_(step(), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / n_e2e
+    cpu = None
+    if not args.no_cpu_baseline and not args.quick:
+        case_cpu = kvgen.mla_prefill_case(s, s, 128, seed=1005, device="cpu")
+        n = 1
+        dt, fl = oracle_prefill_sample(case_cpu, n)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"up-projection of all {s} tokens + the last {n} query row(s), all heads"}
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "us_per_step": ms * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOADS["P-MLA"], "name": "P-MLA", "tokens": s, "heads": 128,
+                       "step": "kvdec_mla_prefill_expand + kvdec_mla_prefill",
+                       "l2": "inputs 14 MB (L2-resident by design: compute-bound)"},
+            "roofline": {"bound": "tensor", "achieved": att_tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                         "frac": att_tf / bf16_peak, "traffic": None, "kernel": "mla_prefill_kernel",
+                         "peak_source": f"{peak_src} bf16_tflops (cuBLAS GEMM, burst)",
+                         "algorithmic_flops_per_launch": fa, "avg_launch_us": att_ms * 1e3},
+            "expand": {"avg_launch_us": exp_ms * 1e3, "tflops": fe / (exp_ms * 1e-3) / 1e12},
+            "cpu_baseline": cpu,
+            "e2e": {"value": (fe + fa) / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": hout.numel() * 4, "ms_per_step": e2e_ms, "steps": n_e2e},
+            "clocks": clocks, "gpu_launches": 3 * args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.config == "P-MLA":
+        if args.gpus != 1 or int(os.environ.get("RANK", "0")) != 0:
+            return
+        bench_prefill(args, reference=args.impl == "reference")
+        return
     if args.impl == "reference":
         run_reference(args)
         return

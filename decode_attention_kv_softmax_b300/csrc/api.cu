@@ -99,6 +99,23 @@ kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
     return KVDEC_OK;
 }
 
+// 3-D bf16 tensor map over [d2][d1][d0] (d0 innermost), 128-byte swizzle.
+kvdec_status encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                       uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t box0, uint32_t box1,
+                       uint32_t box2) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+    return KVDEC_OK;
+}
+
 // ---------------------------------------------------------------- GQA layout
 
 struct GqaPlan {
@@ -502,7 +519,20 @@ kvdec_status kvdec_mla_prefill(const kvdec_mla_prefill_params* p, void* stream) 
     a.out_bf16 = p->out_dtype == KVDEC_BF16;
     const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
     a.scale_log2 = (float)(scale * 1.4426950408889634);
-    cudaError_t e = kvdec::launch_mla_prefill(a, static_cast<cudaStream_t>(stream));
+    a.err = nullptr;
+    a.timeout_ns = kvdec::kDefaultTimeoutNs;
+    // tensor maps: [tokens][heads][dims] for q and the up-projected k, v;
+    // boxes of 64 dims x 1 head x (128 query | 64 key) tokens
+    const uint64_t H = (uint64_t)p->num_heads;
+    kvdec::MlaPrefillMaps maps;
+    kvdec_status st;
+    if ((st = encode_3d(&maps.qn, p->q_nope, 128, H, p->s_q, 256, H * 256, 64, 1, 128)) != KVDEC_OK) return st;
+    if ((st = encode_3d(&maps.qr, p->q_rope, 64, H, p->s_q, 128, H * 128, 64, 1, 128)) != KVDEC_OK) return st;
+    if ((st = encode_3d(&maps.kn, p->k_nope, 128, H, p->s_kv, 256, H * 256, 64, 1, 64)) != KVDEC_OK) return st;
+    if ((st = encode_3d(&maps.v, p->v, 128, H, p->s_kv, 256, H * 256, 64, 1, 64)) != KVDEC_OK) return st;
+    if ((st = encode_2d(&maps.kr, p->k_rope, p->s_kv, 64, 128, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) != KVDEC_OK)
+        return st;
+    cudaError_t e = kvdec::launch_mla_prefill_tc(maps, a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, name);
     return KVDEC_OK;
 }

@@ -235,6 +235,24 @@ KVDEC_DEVINL void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar
         : "memory");
 }
 
+// 3-D tiled TMA load (coordinates innermost first) with an L2 cache hint.
+KVDEC_DEVINL void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2,
+                                   uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+        : "memory");
+}
+
+KVDEC_DEVINL void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
 // 2-D TMA store of a box from (swizzled) shared memory; completion tracked
 // by the issuing thread's bulk groups.
 KVDEC_DEVINL void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {

@@ -101,7 +101,7 @@ struct MlaProjArgs {
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st);
 cudaError_t launch_mla_proj(bool absorb, const MlaProjArgs& a, cudaStream_t st);
 
-// Causal MLA prefill attention on the non-absorbed path (mla_prefill.cu)
+// Causal MLA prefill attention on the non-absorbed path (mla_prefill_tc.cu)
 struct MlaPrefillArgs {
     const __nv_bfloat16* q_nope;   // [s_q, H, 128]
     const __nv_bfloat16* q_rope;   // [s_q, H, 64]
@@ -112,8 +112,16 @@ struct MlaPrefillArgs {
     float* lse;                    // [s_q, H] or null
     int s_q, s_kv, num_heads, kv_offset, out_bf16;
     float scale_log2;
+    uint32_t* err;
+    uint64_t timeout_ns;
 };
-cudaError_t launch_mla_prefill(const MlaPrefillArgs& a, cudaStream_t st);
+// Tensor maps of the tcgen05 prefill: q_nope, q_rope, k_nope, v as 3-D
+// [tokens][heads][dims] (box 64 dims x 1 head x 128 or 64 tokens, 128-byte
+// swizzle), k_rope 2-D [tokens][64] (box 64 x 64).
+struct MlaPrefillMaps {
+    CUtensorMap qn, qr, kn, kr, v;
+};
+cudaError_t launch_mla_prefill_tc(const MlaPrefillMaps& maps, const MlaPrefillArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,

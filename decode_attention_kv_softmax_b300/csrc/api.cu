@@ -470,6 +470,29 @@ kvdec_status kvdec_mla_prefill_expand(const kvdec_mla_expand_params* p, void* st
         return fail(KVDEC_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", name);
     if (p->s < 1 || p->s > (1 << 20) || p->num_heads < 1 || p->num_heads > 65535)
         return fail(KVDEC_ERR_INVALID_ARG, "%s: s %d, num_heads %d", name, p->s, p->num_heads);
+    if (p->num_heads % 2 == 0) {
+        // tcgen05 GEMM: D [s, n_h 128] = c_kv [s, 512] . W^T, W as [n_h 128, 512]
+        const uint64_t N = (uint64_t)p->num_heads * 128;
+        kvdec::MlaExpandMaps maps;
+        kvdec_status st;
+        if ((st = encode_2d(&maps.c, p->c_kv, p->s, 512, 1024, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != KVDEC_OK)
+            return st;
+        if ((st = encode_2d(&maps.wk, p->w_uk, N, 512, 1024, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B)) != KVDEC_OK)
+            return st;
+        if ((st = encode_2d(&maps.wv, p->w_uv, N, 512, 1024, 64, 256, CU_TENSOR_MAP_SWIZZLE_128B)) != KVDEC_OK)
+            return st;
+        kvdec::MlaExpandArgs e;
+        e.k_nope = static_cast<__nv_bfloat16*>(p->k_nope);
+        e.v = static_cast<__nv_bfloat16*>(p->v);
+        e.s = p->s;
+        e.N = (int)N;
+        e.err = nullptr;
+        e.timeout_ns = kvdec::kDefaultTimeoutNs;
+        cudaError_t ce = kvdec::launch_mla_expand_tc(maps, e, static_cast<cudaStream_t>(stream));
+        if (ce != cudaSuccess) return cuda_fail(ce, name);
+        return KVDEC_OK;
+    }
+    // an odd head count: the per-head projection kernel, every head reading the same rows
     kvdec::MlaProjArgs a;
     a.x = static_cast<const __nv_bfloat16*>(p->c_kv);
     a.batch = p->s;

@@ -122,6 +122,21 @@ struct MlaPrefillMaps {
     CUtensorMap qn, qr, kn, kr, v;
 };
 cudaError_t launch_mla_prefill_tc(const MlaPrefillMaps& maps, const MlaPrefillArgs& a, cudaStream_t st);
+
+// Up-projection of a prefill chunk on tcgen05 (mla_expand_tc.cu): maps over
+// c_kv [s, 512] (box 64 x 128) and W_UK, W_UV viewed as [n_h 128, 512]
+// (box 64 x 256), 128-byte swizzle.
+struct MlaExpandMaps {
+    CUtensorMap c, wk, wv;
+};
+struct MlaExpandArgs {
+    __nv_bfloat16* k_nope;   // [s, n_h 128]
+    __nv_bfloat16* v;
+    int s, N;                // N = n_h 128 (a multiple of 256)
+    uint32_t* err;
+    uint64_t timeout_ns;
+};
+cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,

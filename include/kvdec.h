@@ -333,7 +333,9 @@ kvdec_status kvdec_mla_project_out(const kvdec_mla_proj_params* p, void* stream)
  *   k_nope[t, h, :] = W_UK[h] c_kv[t, :],   v[t, h, :] = W_UV[h] c_kv[t, :]
  *   c_kv bf16 [s, 512]; W_UK, W_UV bf16 [num_heads, 128, 512] (as for
  *   kvdec_mla_absorb_q / kvdec_mla_project_out); k_nope, v bf16
- *   [s, num_heads, 128] (fp32 accumulation, one rounding to bf16).
+ *   [s, num_heads, 128] (fp32 accumulation, one rounding to bf16).  An even
+ *   num_heads runs as one tcgen05 GEMM per output, [s, 512] x [512, 128 n_h];
+ *   an odd one on the per-head projection kernel.
  *
  * kvdec_mla_prefill: for every query i (position kv_offset + i) and head h
  *   s_j = scale [q_nope ; q_rope][i, h] . [k_nope[j, h] ; k_rope[j]],

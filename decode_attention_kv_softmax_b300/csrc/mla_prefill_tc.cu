@@ -4,21 +4,33 @@
 // and 128; [ARG] §五.2: FlashAttention's tiled online softmax; §五.3: causal
 // mask).
 //
-// CTA = one head and 128 query rows, 6 warps:
-//   warp 0  TMA producer: Q once (3 boxes of 128 rows x 64 dims), then
-//           64-key K tiles (k_nope 0-63, 64-127, k_rope) and V tiles
-//           (2 boxes of 64 dims) through NS stages;
-//   warp 1  owns TMEM (256 columns) and issues the MMAs from one thread:
-//           S(j) = Q K_j^T into TMEM buffer j mod 2 (12 MMAs of
-//           M=128, N=64, K=16), then O += P(j-1) V_(j-1) (4 MMAs of N=128,
-//           P from shared memory, V MN-major);
+// CTA = one head and 128 query rows, 8 warps.  A cluster pairs the CTAs of
+// two adjacent query blocks of a head, which read the same K/V tiles:
+//   warp 0  TMA producer of Q (3 boxes of 128 rows x 64 dims) and, per
+//           128-key tile, K (k_nope 0-63, 64-127, k_rope) into a 2-stage ring;
+//   warp 6  TMA producer of V (2 boxes of 64 dims) into a 2-stage ring.
+//           For a tile both CTAs need, each loads 64 of its 128 token rows
+//           and multicasts them to both, so L2 serves each tile once per
+//           pair; a stage refills once both CTAs have released it.  A tile
+//           only one CTA needs (the later block's diagonal) it loads alone;
+//   warp 1  owns TMEM and issues S(j) = Q K_j^T into S buffer j mod 2 (12
+//           MMAs of M=128, N=128, K=16; the K stage is released when they
+//           complete);
+//   warp 7  issues O += P(j) V_j (8 MMAs of N=128 with P read from TMEM, V
+//           MN-major; the V stage is released when they complete).  Both
+//           issuers run warp-uniform code and one elected lane issues, and
+//           two issuers halve the serial wait-and-issue chain per tile;
 //   warps 2-5  softmax, one thread per query row (TMEM lane): load S(j),
-//           mask the diagonal and the tail, row max, exponentials into bf16
-//           P (128-byte-swizzled rows in shared memory), row sums; O is
-//           rescaled in TMEM only when a row's max passes its reference
-//           max by more than 2^8 (then after PV(j-1) has completed).
-// S(j+1) runs on the tensor cores while the softmax works on S(j).  All
-// waits are bounded; a timeout sets the error word and unwinds.
+//           mask the diagonal and the tail, row max, exponentials packed to
+//           bf16 pairs into P buffer j mod 2 in TMEM, row sums.  O is
+//           rescaled in TMEM only when a row's max passes its reference max
+//           by more than 2^8 (after PV(j-1) has completed).
+// TMEM columns: S [0,128) and [128,256), O [256,384), P [384,448) and
+// [448,512).  With two S and two P buffers the tensor cores run S(j+1) and
+// PV(j-1) while the softmax works on tile j.  N=128 MMAs run at the tensor
+// cores' full rate where N=64 ones reach about 55 % of it, and a 128-key
+// tile halves the barrier traffic per key.  All waits are bounded; a
+// timeout sets the error word and unwinds.
 #include "common.cuh"
 #include "kernels.h"
 #include "tcgen05.cuh"
@@ -26,58 +38,88 @@
 namespace kvdec {
 
 namespace pft {
-constexpr int kBM = 128, kBN = 64;
-constexpr int kNS = 3;
+constexpr int kBM = 128, kBN = 128;
+constexpr int kNK = 2, kNV = 2;            // K and V ring depths
 constexpr int kQBytes = 3 * 128 * 128;     // 3 boxes [128 rows x 128 B]
-constexpr int kKBox = 64 * 128;            // [64 keys x 128 B]
-constexpr int kStage = 5 * kKBox;          // K: 3 boxes, V: 2 boxes = 40 KB
-constexpr int kPBytes = 128 * 128;         // [128 rows x 64 keys] bf16
+constexpr int kBox = 128 * 128;            // [128 keys x 128 B], loaded as two 64-key halves
+constexpr int kHalf = kBox / 2;
+constexpr int kKStage = 3 * kBox;          // k_nope 0-63, 64-127, k_rope: 48 KB
+constexpr int kVStage = 2 * kBox;          // v 0-63, 64-127: 32 KB
 constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + kNS * kStage;
-constexpr int kOffBars = kOffP + kPBytes;
-enum { B_Q, B_SFULL, B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_PFREE, B_ODONE, B_DONE, B_KV };
-constexpr int kBars = B_KV + 2 * kNS;
+constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffV = kOffK + kNK * kKStage;
+constexpr int kOffBars = kOffV + kNV * kVStage;
+enum {
+    B_Q,
+    B_SFULL,
+    B_SFREE = B_SFULL + 2,
+    B_PFULL = B_SFREE + 2,
+    B_PFREE = B_PFULL + 2,
+    B_ODONE = B_PFREE + 2,
+    B_DONE,
+    B_KFULL,
+    B_KEMPTY = B_KFULL + kNK,
+    B_VFULL = B_KEMPTY + kNK,
+    B_VEMPTY = B_VFULL + kNV,
+    kBars = B_VEMPTY + kNV
+};
 constexpr int kOffMisc = kOffBars + kBars * 8;           // [0] TMEM base, [1] abort word
 constexpr int kSmem = kOffMisc + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;                      // S buffers [0,128), O [128,256)
-constexpr uint32_t kTmemO = 128;
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0, kTmemO = 256, kTmemP = 384;
+
+// key tiles of query block qb (0 for the idle partner of an odd count)
+__device__ __forceinline__ int block_tiles(const MlaPrefillArgs& a, int qb) {
+    if (qb < 0) return 0;
+    const int q0 = qb * kBM;
+    const int kend = min(a.s_kv, a.kv_offset + min(q0 + kBM, a.s_q));
+    return (kend + kBN - 1) / kBN;
+}
 }  // namespace pft
 
-__global__ void __launch_bounds__(192, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
     mla_prefill_tc_kernel(const __grid_constant__ MlaPrefillMaps maps, const MlaPrefillArgs a) {
     using namespace pft;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int qb = gridDim.x - 1 - blockIdx.x;   // heaviest query blocks first
+    const uint32_t rank = cluster_ctarank();
+    // heaviest query blocks first; an odd count leaves the last CTA idle
+    const int G = (a.s_q + kBM - 1) / kBM;
+    const int qb = G - 1 - (int)blockIdx.x;
     const int hh = blockIdx.y;
     const int q0 = qb * kBM;
-    const int kend = min(a.s_kv, a.kv_offset + min(q0 + kBM, a.s_q));
-    const int nt = (kend + kBN - 1) / kBN;      // >= 1: kv_offset >= 0
+    const int nt = block_tiles(a, qb);
+    const int shared = min(nt, block_tiles(a, G - 1 - (int)(blockIdx.x ^ 1u)));   // tiles of both CTAs
+    constexpr uint16_t kBoth = 0x3;
 
     const uint32_t bar0 = smem_addr(smem + kOffBars);
     auto bar = [bar0](int i) { return bar0 + 8u * (uint32_t)i; };
-    auto kv_full = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + s); };
-    auto kv_empty = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + kNS + s); };
     volatile int* misc = reinterpret_cast<volatile int*>(smem + kOffMisc);
     volatile int* abort_word = misc + 1;
-    const uint32_t sQ = smem_addr(smem + kOffQ), sKV = smem_addr(smem + kOffKV), sP = smem_addr(smem + kOffP);
+    const uint32_t sQ = smem_addr(smem + kOffQ), sK = smem_addr(smem + kOffK), sV = smem_addr(smem + kOffV);
 
     if (tid == 0) {
         mbar_init(bar(B_Q), 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar(B_SFULL + i), 1);
             mbar_init(bar(B_SFREE + i), 4);
+            mbar_init(bar(B_PFULL + i), 4);
+            mbar_init(bar(B_PFREE + i), 1);
         }
-        mbar_init(bar(B_PFULL), 4);
-        mbar_init(bar(B_PFREE), 1);
         mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_DONE), 1);
-        for (int s = 0; s < kNS; ++s) {
-            mbar_init(kv_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+        // a stage is released by both CTAs of the pair (a tile only this CTA
+        // reads is released twice by it)
+        for (int s = 0; s < kNK; ++s) {
+            mbar_init(bar(B_KFULL + s), 1);
+            mbar_init(bar(B_KEMPTY + s), 2);
+        }
+        for (int s = 0; s < kNV; ++s) {
+            mbar_init(bar(B_VFULL + s), 1);
+            mbar_init(bar(B_VEMPTY + s), 2);
         }
         misc[1] = 0;
         fence_barrier_init();
@@ -89,85 +131,147 @@ __global__ void __launch_bounds__(192, 1)
     }
     __syncthreads();
     tc_fence_after();
+    cluster_sync_all();                                    // the peer's barriers exist
     const uint32_t tmem = (uint32_t)misc[0];
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (nt > 0 && (warp == 0 || warp == 6)) {
+        // ------------------------------------------------------- producers
         if (lane == 0) {
-            prefetch_tensormap(&maps.qn);
-            prefetch_tensormap(&maps.qr);
-            prefetch_tensormap(&maps.kn);
-            prefetch_tensormap(&maps.kr);
-            prefetch_tensormap(&maps.v);
+            const bool is_k = warp == 0;
             const uint64_t keep = l2_policy_evict_last();   // K/V are read by every query block
-            mbar_arrive_expect_tx(bar(B_Q), kQBytes);
-            tma_load_3d(sQ, &maps.qn, bar(B_Q), 0, hh, q0);
-            tma_load_3d(sQ + 16384, &maps.qn, bar(B_Q), 64, hh, q0);
-            tma_load_3d(sQ + 32768, &maps.qr, bar(B_Q), 0, hh, q0);
+            if (is_k) {
+                prefetch_tensormap(&maps.qn);
+                prefetch_tensormap(&maps.qr);
+                prefetch_tensormap(&maps.kn);
+                prefetch_tensormap(&maps.kr);
+                mbar_arrive_expect_tx(bar(B_Q), kQBytes);
+                tma_load_3d(sQ, &maps.qn, bar(B_Q), 0, hh, q0);
+                tma_load_3d(sQ + 16384, &maps.qn, bar(B_Q), 64, hh, q0);
+                tma_load_3d(sQ + 32768, &maps.qr, bar(B_Q), 0, hh, q0);
+            } else {
+                prefetch_tensormap(&maps.v);
+            }
+            const int NS = is_k ? kNK : kNV;
+            const int empty0 = is_k ? B_KEMPTY : B_VEMPTY, full0 = is_k ? B_KFULL : B_VFULL;
+            const int stage_bytes = is_k ? kKStage : kVStage;
+            const uint32_t ring = is_k ? sK : sV;
             int issued = 0;
             for (int j = 0; j < nt; ++j) {
-                const int s = j % kNS;
-                if (!wait_or_abort(kv_empty(s), (uint32_t)(((j / kNS) & 1) ^ 1), abort_word, a.err, a.timeout_ns))
+                const int k0 = j * kBN, st = j % NS;
+                const uint32_t ep = (uint32_t)(((j / NS) & 1) ^ 1);
+                if (!mbar_try_wait_acq_cluster(bar(empty0 + st), ep) &&
+                    !wait_cluster_or_abort(bar(empty0 + st), ep, abort_word, a.err, a.timeout_ns))
                     break;
-                const uint32_t fb = kv_full(s), dst = sKV + s * kStage;
-                mbar_arrive_expect_tx(fb, kStage);
-                const int k0 = j * kBN;
-                tma_load_3d_hint(dst, &maps.kn, fb, 0, hh, k0, keep);
-                tma_load_3d_hint(dst + kKBox, &maps.kn, fb, 64, hh, k0, keep);
-                tma_load_2d(dst + 2 * kKBox, &maps.kr, fb, 0, k0, keep);
-                tma_load_3d_hint(dst + 3 * kKBox, &maps.v, fb, 0, hh, k0, keep);
-                tma_load_3d_hint(dst + 4 * kKBox, &maps.v, fb, 64, hh, k0, keep);
+                const uint32_t fb = bar(full0 + st), dst = ring + st * stage_bytes;
+                mbar_arrive_expect_tx(fb, stage_bytes);
+                if (j < shared) {
+                    // this CTA's half of the token rows, to both CTAs
+                    const uint32_t d = dst + rank * kHalf;
+                    const int t = k0 + 64 * (int)rank;
+                    if (is_k) {
+                        tma_load_3d_mc(d, &maps.kn, fb, 0, hh, t, kBoth, keep);
+                        tma_load_3d_mc(d + kBox, &maps.kn, fb, 64, hh, t, kBoth, keep);
+                        tma_load_2d_mc(d + 2 * kBox, &maps.kr, fb, 0, t, kBoth, keep);
+                    } else {
+                        tma_load_3d_mc(d, &maps.v, fb, 0, hh, t, kBoth, keep);
+                        tma_load_3d_mc(d + kBox, &maps.v, fb, 64, hh, t, kBoth, keep);
+                    }
+                } else {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t d = dst + h * kHalf;
+                        const int t = k0 + 64 * h;
+                        if (is_k) {
+                            tma_load_3d_hint(d, &maps.kn, fb, 0, hh, t, keep);
+                            tma_load_3d_hint(d + kBox, &maps.kn, fb, 64, hh, t, keep);
+                            tma_load_2d(d + 2 * kBox, &maps.kr, fb, 0, t, keep);
+                        } else {
+                            tma_load_3d_hint(d, &maps.v, fb, 0, hh, t, keep);
+                            tma_load_3d_hint(d + kBox, &maps.v, fb, 64, hh, t, keep);
+                        }
+                    }
+                }
                 ++issued;
             }
-            // never leave TMA writes in flight
-            if (!mbar_wait_bounded(bar(B_Q), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
-            for (int i = (issued > kNS ? issued - kNS : 0); i < issued; ++i)
-                if (!mbar_wait_bounded(kv_full(i % kNS), (uint32_t)((i / kNS) & 1), a.timeout_ns)) {
+            // never leave TMA writes in flight (the peer's halves included)
+            if (is_k && !mbar_wait_bounded(bar(B_Q), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+            for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
+                if (!mbar_wait_bounded(bar(full0 + i % NS), (uint32_t)((i / NS) & 1), a.timeout_ns)) {
                     report(a.err, KVDEC_DEVERR_TIMEOUT);
                     break;
                 }
-        }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t iS = umma_idesc_bf16(128, 64, false, false);
-            constexpr uint32_t iP = umma_idesc_bf16(128, 128, false, true);
-            auto pv = [&](int j) -> bool {
-                if (!wait_or_abort(bar(B_PFULL), (uint32_t)(j & 1), abort_word, a.err, a.timeout_ns)) return false;
-                tc_fence_after();
-                const uint32_t vb = sKV + (j % kNS) * kStage + 3 * kKBox;
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16_ss(tmem + kTmemO, umma_desc(sP + ks * 32, 16, 1024, kSwizzle128B),
-                                 umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
-                                 (j > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(bar(B_PFREE));
-                umma_commit(kv_empty(j % kNS));
-                return true;
-            };
-            bool ok = wait_or_abort(bar(B_Q), 0, abort_word, a.err, a.timeout_ns);
-            for (int j = 0; ok && j < nt; ++j) {
-                const int s = j % kNS, sb = j & 1;
-                if (!wait_or_abort(kv_full(s), (uint32_t)((j / kNS) & 1), abort_word, a.err, a.timeout_ns)) break;
-                if (j >= 2 && !wait_or_abort(bar(B_SFREE + sb), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
-                                             a.timeout_ns))
+            // the peer's last releases of shared tiles have landed here (the
+            // earlier ones were waited for before refilling their stages)
+            for (int i = max(0, nt - NS); i < shared; ++i)
+                if (!wait_cluster_or_abort(bar(empty0 + i % NS), (uint32_t)((i / NS) & 1), abort_word, a.err,
+                                           a.timeout_ns))
                     break;
-                tc_fence_after();
-                const uint32_t kb = sKV + s * kStage;
-                for (int ks = 0; ks < 12; ++ks)
-                    umma_bf16_ss(tmem + 64u * sb,
-                                 umma_desc(sQ + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, kSwizzle128B),
-                                 umma_desc(kb + (ks >> 2) * kKBox + (ks & 3) * 32, 16, 1024, kSwizzle128B), iS,
-                                 ks > 0 ? 1u : 0u);
-                umma_commit(bar(B_SFULL + sb));
-                if (j >= 1 && !pv(j - 1)) ok = false;
-            }
-            if (ok) pv(nt - 1);
-            umma_commit(bar(B_ODONE));
-            // every MMA issued by this thread has completed before TMEM is freed
-            umma_commit(bar(B_DONE));
-            if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
-    } else {
+    } else if (nt > 0 && (warp == 1 || warp == 7)) {
+        // ------------------------------------------------------- MMA issuers
+        // warp 1 issues S(j) = Q K_j^T, warp 7 O += P(j) V_j.  Each whole warp
+        // runs its loop (warp-uniform operands) and one elected lane issues
+        // each MMA and commit; a commit covers the MMAs of its own warp.
+        // Descriptors are a base plus constant offsets (16-byte units; no
+        // carry out of the 14-bit address field below 256 KB).
+        auto wait1 = [&](uint32_t b, uint32_t par) -> bool {
+            if (__all_sync(0xffffffffu, mbar_try_wait(b, par) ? 1 : 0)) return true;
+            int ok = 1;
+            if (lane == 0) ok = wait_or_abort(b, par, abort_word, a.err, a.timeout_ns) ? 1 : 0;
+            return __all_sync(0xffffffffu, ok) != 0;
+        };
+        // release a ring stage: to both CTAs for a shared tile, else twice here
+        auto release = [&](uint32_t b, int j) {
+            if (j < shared) {
+                umma_commit_mc_w(b, kBoth);
+            } else {
+                umma_commit_w(b);
+                umma_commit_w(b);
+            }
+        };
+        if (warp == 1) {
+            constexpr uint32_t iS = umma_idesc_bf16(128, 128, false, false);
+            const uint64_t dQ = umma_desc(sQ, 16, 1024, kSwizzle128B);
+            const uint64_t dK = umma_desc(sK, 16, 1024, kSwizzle128B);
+            bool ok = wait1(bar(B_Q), 0);
+            for (int j = 0; ok && j < nt; ++j) {
+                const int ks_ = j % kNK, sb = j & 1;
+                if (!wait1(bar(B_KFULL + ks_), (uint32_t)((j / kNK) & 1))) break;
+                if (j >= 2 && !wait1(bar(B_SFREE + sb), (uint32_t)(((j - 2) >> 1) & 1))) break;
+                tc_fence_after();
+                const uint64_t dk = dK + (uint64_t)((ks_ * kKStage) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < 12; ++ks)
+                    umma_bf16_ss_w(tmem + kTmemS + 128u * sb,
+                                   dQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
+                                   dk + (uint64_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4), iS, ks > 0 ? 1u : 0u);
+                umma_commit_w(bar(B_SFULL + sb));
+                release(bar(B_KEMPTY + ks_), j);
+            }
+            // every MMA of this warp has completed before TMEM is freed
+            umma_commit_w(bar(B_DONE));
+            if (lane == 0 && !mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+        } else {
+            constexpr uint32_t iP = umma_idesc_bf16(128, 128, false, true);
+            const uint64_t dV = umma_desc(sV, kBox, 1024, kSwizzle128B);
+            for (int j = 0; j < nt; ++j) {
+                const int pb = j & 1, vs = j % kNV;
+                if (!wait1(bar(B_PFULL + pb), (uint32_t)((j >> 1) & 1))) break;
+                if (!wait1(bar(B_VFULL + vs), (uint32_t)((j / kNV) & 1))) break;
+                tc_fence_after();
+                const uint64_t dv = dV + (uint64_t)((vs * kVStage) >> 4);
+#pragma unroll
+                for (int ks = 0; ks < kBN / 16; ++ks)
+                    umma_bf16_ts_w(tmem + kTmemO, tmem + kTmemP + 64u * pb + 8u * ks,
+                                   dv + (uint64_t)((ks * 2048) >> 4), iP, (j > 0 || ks > 0) ? 1u : 0u);
+                umma_commit_w(bar(B_PFREE + pb));
+                release(bar(B_VEMPTY + vs), j);
+            }
+            // O is final (or the loop was abandoned) once every PV has completed
+            umma_commit_w(bar(B_ODONE));
+            if (lane == 0 && !mbar_wait_bounded(bar(B_ODONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+        }
+    } else if (nt > 0 && warp >= 2 && warp <= 5) {
         // ------------------------------------------------------------ softmax
         const int qd = warp & 3;                 // TMEM lane quadrant of this warp
         const int row = 32 * qd + lane;          // query row in the block
@@ -175,15 +279,18 @@ __global__ void __launch_bounds__(192, 1)
         const int qpos = a.kv_offset + q0 + row; // this row's position
         const float sl2 = a.scale_log2;
         float m_ref = -INFINITY, l = 0.f;
-        uint8_t* prow = smem + kOffP + row * 128;
+        // completed phases are checked first (no abort-word load on that path)
+        auto waitf = [&](uint32_t b, uint32_t par) -> bool {
+            return mbar_try_wait(b, par) || wait_or_abort(b, par, abort_word, a.err, a.timeout_ns);
+        };
         for (int j = 0; j < nt; ++j) {
             const int sb = j & 1;
-            if (!wait_or_abort(bar(B_SFULL + sb), (uint32_t)((j >> 1) & 1), abort_word, a.err, a.timeout_ns)) break;
+            if (!waitf(bar(B_SFULL + sb), (uint32_t)((j >> 1) & 1))) break;
             tc_fence_after();
-            float s[64];
+            float s[kBN];
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-                tmem_ld16(trow + 64u * sb + 16 * c, *reinterpret_cast<float(*)[16]>(s + 16 * c));
+            for (int c = 0; c < kBN / 16; ++c)
+                tmem_ld16(trow + kTmemS + 128u * sb + 16 * c, *reinterpret_cast<float(*)[16]>(s + 16 * c));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -192,25 +299,26 @@ __global__ void __launch_bounds__(192, 1)
             const int kp0 = j * kBN;
             if (kp0 + kBN - 1 > a.kv_offset + q0 || kp0 + kBN > a.s_kv) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c)
+                for (int c = 0; c < kBN; ++c)
                     if (kp0 + c > qpos || kp0 + c >= a.s_kv) s[c] = -INFINITY;
             }
             float mt[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mt[i] = fmaxf(s[i], s[i + 32]);
+            for (int i = 0; i < 32; ++i) mt[i] = fmaxf(fmaxf(s[i], s[i + 32]), fmaxf(s[i + 64], s[i + 96]));
 #pragma unroll
             for (int w2 = 16; w2 >= 1; w2 >>= 1)
 #pragma unroll
                 for (int i = 0; i < w2; ++i) mt[i] = fmaxf(mt[i], mt[i + w2]);
             const float mx = mt[0] * sl2;
-            // P(j-1) has been consumed (and O holds PV(j-1)) before P(j) or a rescale
-            if (j >= 1 && !wait_or_abort(bar(B_PFREE), (uint32_t)((j - 1) & 1), abort_word, a.err, a.timeout_ns))
-                break;
             if (mx > m_ref + 8.f) {
-                // new reference max: rescale the running sum and, after a PV, O
+                // new reference max: rescale the running sum and, once O holds
+                // PV(j-1), O itself
                 const float alpha = (m_ref == -INFINITY) ? 0.f : fast_exp2(m_ref - mx);
                 l *= alpha;
                 if (j >= 1) {
+                    if (!wait_or_abort(bar(B_PFREE + ((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word,
+                                       a.err, a.timeout_ns))
+                        break;
                     tc_fence_after();
 #pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
@@ -225,25 +333,27 @@ __global__ void __launch_bounds__(192, 1)
                 }
                 m_ref = mx;
             }
+            // P buffer sb is free once PV(j-2) has completed
+            if (j >= 2 && !waitf(bar(B_PFREE + sb), (uint32_t)(((j - 2) >> 1) & 1))) break;
             const float b = (m_ref == -INFINITY) ? 0.f : m_ref;
             float ls = 0.f;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                uint32_t pk[4];
+            for (int h = 0; h < kBN / 32; ++h) {
+                uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float p0 = fast_exp2(fmaf(s[8 * k + 2 * e], sl2, -b));
-                    const float p1 = fast_exp2(fmaf(s[8 * k + 2 * e + 1], sl2, -b));
+                for (int e = 0; e < 16; ++e) {
+                    const float p0 = fast_exp2(fmaf(s[32 * h + 2 * e], sl2, -b));
+                    const float p1 = fast_exp2(fmaf(s[32 * h + 2 * e + 1], sl2, -b));
                     ls += p0 + p1;
                     pk[e] = pack_bf16x2(p0, p1);
                 }
-                *reinterpret_cast<uint4*>(prow + ((k ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                tmem_st16u(trow + kTmemP + 64u * sb + 16 * h, pk);
             }
             l += ls;
-            fence_proxy_async();
+            tmem_st_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(B_PFULL));
+            if (lane == 0) mbar_arrive(bar(B_PFULL + sb));
         }
         // ---- O / l out
         if (wait_or_abort(bar(B_ODONE), 0, abort_word, a.err, a.timeout_ns)) {
@@ -282,6 +392,8 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
+    asm volatile("fence.acq_rel.cluster;" ::: "memory");
+    cluster_sync_all();   // the peer no longer touches this CTA's shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -289,12 +401,15 @@ __global__ void __launch_bounds__(192, 1)
 }
 
 cudaError_t launch_mla_prefill_tc(const MlaPrefillMaps& maps, const MlaPrefillArgs& a, cudaStream_t st) {
-    const dim3 grid((a.s_q + pft::kBM - 1) / pft::kBM, a.num_heads);
+    // query blocks in pairs (cluster of two); an odd count gets an idle partner
+    const int G = (a.s_q + pft::kBM - 1) / pft::kBM;
+    const dim3 grid((G + 1) & ~1, a.num_heads);
     cudaError_t e = cudaFuncSetAttribute(mla_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pft::kSmem);
     if (e != cudaSuccess) return e;
-    mla_prefill_tc_kernel<<<grid, 192, pft::kSmem, st>>>(maps, a);
+    mla_prefill_tc_kernel<<<grid, pft::kThreads, pft::kSmem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
 }  // namespace kvdec
+

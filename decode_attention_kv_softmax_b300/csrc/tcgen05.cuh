@@ -103,6 +103,45 @@ KVDEC_DEVINL void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc
         : "memory");
 }
 
+// Warp-wide forms: every lane of the warp executes the call with the same
+// (warp-uniform) operands and one elected lane issues.  Keeping the issuing
+// code warp-uniform lets the descriptors stay in uniform registers, which
+// the single-lane forms above cannot; the whole warp must be converged.
+KVDEC_DEVINL void umma_bf16_ss_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+KVDEC_DEVINL void umma_bf16_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+KVDEC_DEVINL void umma_commit_w(uint32_t mbar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(mbar)
+        : "memory");
+}
+
+// Warp-wide commit that arrives on the mbarrier at `mbar`'s offset in each
+// CTA of the cluster named in `mask`.
+KVDEC_DEVINL void umma_commit_mc_w(uint32_t mbar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(mbar),
+        "h"(mask)
+        : "memory");
+}
+
 // Warp-collective store of 16 32-bit columns per lane (raw bits).
 KVDEC_DEVINL void tmem_st16u(uint32_t taddr, const uint32_t (&v)[16]) {
     asm volatile(

@@ -376,6 +376,13 @@ KVDEC_DEVINL uint32_t bf16x2_to_f16x2(uint32_t u) {
 // ---------------------------------------------------------------- numerics
 
 // 2^x on the special-function unit (ex2.approx: a PTX instruction).
+// Three-input maximum (one instruction on sm_100 and later).
+KVDEC_DEVINL float fmax3f(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 KVDEC_DEVINL float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

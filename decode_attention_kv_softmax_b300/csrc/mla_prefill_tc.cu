@@ -289,8 +289,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
             tc_fence_after();
             float s[kBN];
 #pragma unroll
-            for (int c = 0; c < kBN / 16; ++c)
-                tmem_ld16(trow + kTmemS + 128u * sb + 16 * c, *reinterpret_cast<float(*)[16]>(s + 16 * c));
+            for (int c = 0; c < kBN / 32; ++c)
+                tmem_ld32(trow + kTmemS + 128u * sb + 32 * c, *reinterpret_cast<float(*)[32]>(s + 32 * c));
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
@@ -302,14 +302,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
                 for (int c = 0; c < kBN; ++c)
                     if (kp0 + c > qpos || kp0 + c >= a.s_kv) s[c] = -INFINITY;
             }
+            // row max: three-input maxima, 128 -> 32 -> 11 -> 4 -> 1
             float mt[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mt[i] = fmaxf(fmaxf(s[i], s[i + 32]), fmaxf(s[i + 64], s[i + 96]));
+            for (int i = 0; i < 32; ++i) mt[i] = fmaxf(fmax3f(s[i], s[i + 32], s[i + 64]), s[i + 96]);
+            float m2[11];
 #pragma unroll
-            for (int w2 = 16; w2 >= 1; w2 >>= 1)
-#pragma unroll
-                for (int i = 0; i < w2; ++i) mt[i] = fmaxf(mt[i], mt[i + w2]);
-            const float mx = mt[0] * sl2;
+            for (int i = 0; i < 10; ++i) m2[i] = fmax3f(mt[3 * i], mt[3 * i + 1], mt[3 * i + 2]);
+            m2[10] = fmaxf(mt[30], mt[31]);
+            const float m3a = fmax3f(m2[0], m2[1], m2[2]), m3b = fmax3f(m2[3], m2[4], m2[5]);
+            const float m3c = fmax3f(m2[6], m2[7], m2[8]), m3d = fmaxf(m2[9], m2[10]);
+            const float mx = fmaxf(fmax3f(m3a, m3b, m3c), m3d) * sl2;
             if (mx > m_ref + 8.f) {
                 // new reference max: rescale the running sum and, once O holds
                 // PV(j-1), O itself
@@ -336,20 +339,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
             // P buffer sb is free once PV(j-2) has completed
             if (j >= 2 && !waitf(bar(B_PFREE + sb), (uint32_t)(((j - 2) >> 1) & 1))) break;
             const float b = (m_ref == -INFINITY) ? 0.f : m_ref;
-            float ls = 0.f;
+            // p = 2^(s sl2 - b) with packed f32x2 FMAs and adds (two keys each)
+            const float2 sl2x2 = make_float2(sl2, sl2), nbx2 = make_float2(-b, -b);
+            float2 ls2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int h = 0; h < kBN / 32; ++h) {
-                uint32_t pk[16];
+            for (int h = 0; h < kBN / 64; ++h) {
+                uint32_t pk[32];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float p0 = fast_exp2(fmaf(s[32 * h + 2 * e], sl2, -b));
-                    const float p1 = fast_exp2(fmaf(s[32 * h + 2 * e + 1], sl2, -b));
-                    ls += p0 + p1;
-                    pk[e] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 32; ++e) {
+                    const float2 x = __ffma2_rn(make_float2(s[64 * h + 2 * e], s[64 * h + 2 * e + 1]), sl2x2, nbx2);
+                    const float2 p = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    ls2 = __fadd2_rn(ls2, p);
+                    pk[e] = pack_bf16x2(p.x, p.y);
                 }
-                tmem_st16u(trow + kTmemP + 64u * sb + 16 * h, pk);
+                tmem_st32u(trow + kTmemP + 64u * sb + 32 * h, pk);
             }
-            l += ls;
+            l += ls2.x + ls2.y;
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

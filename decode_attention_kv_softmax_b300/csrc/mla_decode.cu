@@ -207,46 +207,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         // ------------------------------------------------------------ S issuer
         // S(j) goes to TMEM buffer j & 1 once its page and Q are there and the
         // softmax has read S(j-2) out of that buffer.  PV has its own issuer
-        // (the last warp), so that a PV never queues behind a later S.
-        // Blocking waits park the thread.
-        if (lane == 0 && n > 0) {
+        // (the last warp), so that a PV never queues behind a later S.  Both
+        // issuers run their loops on the whole warp (warp-uniform operands,
+        // descriptors as a base plus constant offsets) and one elected lane
+        // issues each MMA and commit; lane 0 parks in the slow waits.
+        if (n > 0) {
             constexpr uint32_t iS = umma_idesc_bf16(128, 64, false, false);
+            const uint64_t dK = umma_desc(sKV, 16, 1024, kSwizzle128B);
+            const uint64_t dKR = umma_desc(sKV + 32768, 16, 512, kSwizzle64B);
+            const uint64_t dQR = umma_desc(sQR, 16, 512, kSwizzle64B);
+            auto wait1 = [&](uint32_t bb, uint32_t par) -> bool {
+                if (__all_sync(0xffffffffu, mbar_try_wait(bb, par) ? 1 : 0)) return true;
+                int ok = 1;
+                if (lane == 0) ok = wait_or_abort(bb, par, abort_word, a.err, a.timeout_ns) ? 1 : 0;
+                return __all_sync(0xffffffffu, ok) != 0;
+            };
             TileCursor cs;
             cs.start(S, t_begin);
             uint32_t seg_s = 0;                  // sequences started so far
             for (long long j = 0; j < n; ++j) {
-                if ((j == 0 || cs.lt == 0) &&
-                    !wait_or_abort(bar(B_Q_FULL), (seg_s++) & 1u, abort_word, a.err, a.timeout_ns))
-                    break;
+                if ((j == 0 || cs.lt == 0) && !wait1(bar(B_Q_FULL), (seg_s++) & 1u)) break;
                 const int stage = (int)(j % NS);
                 const int sb = (int)(j & 1);
-                if (!wait_or_abort(kv_full(stage), (uint32_t)((j / NS) & 1), abort_word, a.err, a.timeout_ns)) break;
-                if (j >= 2 && !wait_or_abort(bar(B_S_FREE + sb), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
-                                             a.timeout_ns))
-                    break;
+                if (!wait1(kv_full(stage), (uint32_t)((j / NS) & 1))) break;
+                if (j >= 2 && !wait1(bar(B_S_FREE + sb), (uint32_t)(((j - 2) >> 1) & 1))) break;
                 tc_fence_after();
-                const uint32_t kb = sKV + stage * kStageBytes;
+                const uint64_t so = (uint64_t)((stage * kStageBytes) >> 4);
                 const uint32_t d = tmem + kTmemS + 64u * sb;
+#pragma unroll
                 for (int q = 0; q < 16; ++q)
-                    umma_bf16_ts(d, tmem + kTmemQ + 8 * q,
-                                 umma_desc(kb + (q >> 2) * 8192 + (q & 3) * 32, 16, 1024, kSwizzle128B), iS, q > 0);
+                    umma_bf16_ts_w(d, tmem + kTmemQ + 8 * q, dK + so + (uint64_t)(((q >> 2) * 8192 + (q & 3) * 32) >> 4),
+                                   iS, q > 0 ? 1u : 0u);
+#pragma unroll
                 for (int q = 0; q < 2; ++q)
-                    umma_bf16_ss(d, umma_desc(sQR + q * 32, 16, 512, kSwizzle64B),
-                                 umma_desc(kb + 32768 + q * 32, 16, 512, kSwizzle64B), iS, 1u);
-                umma_commit(bar(B_S_FULL + sb));
+                    umma_bf16_ss_w(d, dQR + (uint64_t)((q * 32) >> 4), dKR + so + (uint64_t)((q * 32) >> 4), iS, 1u);
+                umma_commit_w(bar(B_S_FULL + sb));
                 cs.advance(S);
             }
-            // every MMA issued by this thread has completed before TMEM is freed
-            umma_commit(bar(B_DONE));
-            if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+            // every MMA issued by this warp has completed before TMEM is freed
+            umma_commit_w(bar(B_DONE));
+            if (lane == 0 && !mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
     } else if (warp == kSoftWarps + 2) {
         // ------------------------------------------------------------ PV issuer
         // PV(j) once P(j) is in shared memory (and, at a sequence's first page,
         // once the previous sequence's O has been flushed); then the page's
         // stage goes back to the producer.
-        if (lane == 0 && n > 0) {
+        if (n > 0) {
             constexpr uint32_t iP = umma_idesc_bf16(128, 256, false, true);
+            const uint64_t dP = umma_desc(sP, 16, 1024, kSwizzle128B);
+            const uint64_t dV = umma_desc(sKV, 8192, 1024, kSwizzle128B);
+            auto wait1 = [&](uint32_t bb, uint32_t par) -> bool {
+                if (__all_sync(0xffffffffu, mbar_try_wait(bb, par) ? 1 : 0)) return true;
+                int ok = 1;
+                if (lane == 0) ok = wait_or_abort(bb, par, abort_word, a.err, a.timeout_ns) ? 1 : 0;
+                return __all_sync(0xffffffffu, ok) != 0;
+            };
             TileCursor cp;
             cp.start(S, t_begin);
             uint32_t seg_p = 0;                  // sequences started so far
@@ -254,24 +270,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 const bool first = (j == 0) || cp.lt == 0;
                 if (first) ++seg_p;
                 const int pb = (int)(j & 1);
-                if (!wait_or_abort(bar(B_P_FULL + pb), (uint32_t)((j >> 1) & 1), abort_word, a.err, a.timeout_ns))
-                    break;
-                if (first && seg_p > 1 &&
-                    !wait_or_abort(bar(B_O_FREE), (seg_p - 2) & 1u, abort_word, a.err, a.timeout_ns))
-                    break;
+                if (!wait1(bar(B_P_FULL + pb), (uint32_t)((j >> 1) & 1))) break;
+                if (first && seg_p > 1 && !wait1(bar(B_O_FREE), (seg_p - 2) & 1u)) break;
                 tc_fence_after();
                 const int pst = (int)(j % NS);
-                const uint32_t vb = sKV + pst * kStageBytes;
+                const uint64_t po = (uint64_t)(((PB == 2 ? pb * kPBytes : 0)) >> 4);
+                const uint64_t vo = (uint64_t)((pst * kStageBytes) >> 4);
+#pragma unroll
                 for (int ks = 0; ks < 4; ++ks)
-                    umma_bf16_ss(tmem + kTmemO, umma_desc(sP + (PB == 2 ? pb * kPBytes : 0) + ks * 32, 16, 1024, kSwizzle128B),
-                                 umma_desc(vb + ks * 2048, 8192, 1024, kSwizzle128B), iP,
-                                 (first && ks == 0) ? 0u : 1u);
-                umma_commit(bar(B_PV_DONE + pb));
-                umma_commit(kv_empty(pst));
+                    umma_bf16_ss_w(tmem + kTmemO, dP + po + (uint64_t)((ks * 32) >> 4),
+                                   dV + vo + (uint64_t)((ks * 2048) >> 4), iP, (first && ks == 0) ? 0u : 1u);
+                umma_commit_w(bar(B_PV_DONE + pb));
+                umma_commit_w(kv_empty(pst));
                 cp.advance(S);
             }
-            umma_commit(bar(B_DONE));
-            if (!mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
+            umma_commit_w(bar(B_DONE));
+            if (lane == 0 && !mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
     } else {
         // ------------------------------------------------------------ softmax groups

@@ -438,7 +438,10 @@ def bench_prefill(args, reference=False):
                        "step": "kvdec_mla_prefill_expand + kvdec_mla_prefill",
                        "l2": "inputs 14 MB (L2-resident by design: compute-bound)"},
             "roofline": {"bound": "tensor", "achieved": att_tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                         "frac": att_tf / bf16_peak, "traffic": None, "kernel": "mla_prefill_kernel",
+                         "frac": att_tf / bf16_peak,
+                         "traffic": ncu_traffic("mla_prefill_tc_kernel",
+                                                ["mla_prefill_tc.cu", "common.cuh", "tcgen05.cuh"]),
+                         "kernel": "mla_prefill_tc_kernel",
                          "peak_source": f"{peak_src} bf16_tflops (cuBLAS GEMM, burst)",
                          "algorithmic_flops_per_launch": fa, "avg_launch_us": att_ms * 1e3},
             "expand": {"avg_launch_us": exp_ms * 1e3, "tflops": fe / (exp_ms * 1e-3) / 1e12},
@@ -601,7 +604,7 @@ def main():
     dec_alg = sum(dec_bytes[i & 1] for i in range(args.steps)) / args.steps
     achieved = dec_alg / (dec_avg_ms * 1e-3) / 1e9
 
-    kfile = ["mla_decode.cu", "common.cuh", "schedule.cuh"] if mla else \
+    kfile = ["mla_decode.cu", "common.cuh", "schedule.cuh", "tcgen05.cuh"] if mla else \
         ["gqa_decode.cu", "common.cuh", "schedule.cuh"]
     kname = "mla_decode_kernel" if mla else "gqa_decode_kernel"
     tkey = kname + ("[fp8]" if fp8 else "")     # the FP8 instantiation has its own counters

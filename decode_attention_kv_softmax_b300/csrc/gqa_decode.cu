@@ -494,16 +494,24 @@ __global__ void __launch_bounds__(160, 2)
                     int w0, kind0;
                     S.first_piece(cur.b, cur.j, w0, kind0);
                     if (tid < nrows) {
-                        float M = -INFINITY;
-                        for (int s2 = 0; s2 < np; ++s2) {
-                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                            M = fmaxf(M, __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid));
-                        }
-                        float den = 0.f;
-                        for (int s2 = 0; s2 < np; ++s2) {
-                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                            const float ls = __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid);
-                            den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                        // max and denominator in one pass, four pieces' loads in flight
+                        float M = -INFINITY, den = 0.f;
+                        for (int s2 = 0; s2 < np; s2 += 4) {
+                            float ls[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int sp = s2 + u;
+                                const int sl = 2 * (w0 + sp) + (sp == 0 ? kind0 : 0);
+                                ls[u] = sp < np ? __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid) : -INFINITY;
+                            }
+                            const float Mn = fmaxf(fmaxf(M, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
+                            if (Mn != -INFINITY) {
+                                den = (M == -INFINITY) ? 0.f : den * fast_exp2((M - Mn) * kLog2e);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    den += (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - Mn) * kLog2e);
+                                M = Mn;
+                            }
                         }
                         rowml[tid * 2] = M;
                         rowml[tid * 2 + 1] = den;
@@ -516,16 +524,28 @@ __global__ void __launch_bounds__(160, 2)
                         const float M = rowml[r * 2], den = rowml[r * 2 + 1];
                         const float inv = den > 0.f ? 1.f / den : 0.f;
                         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                        for (int s2 = 0; s2 < np; ++s2) {
-                            const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                            const float ls = __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r);
-                            const float wgt = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * inv;
-                            const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                a.part_o + ((size_t)sl * a.hc_rows + r) * D + c4 * 4));
-                            acc.x = fmaf(wgt, v.x, acc.x);
-                            acc.y = fmaf(wgt, v.y, acc.y);
-                            acc.z = fmaf(wgt, v.z, acc.z);
-                            acc.w = fmaf(wgt, v.w, acc.w);
+                        // four pieces' loads in flight per round trip
+                        for (int s2 = 0; s2 < np; s2 += 4) {
+                            float ls[4];
+                            float4 v[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int sp = s2 + u;
+                                const int sl = 2 * (w0 + sp) + (sp == 0 ? kind0 : 0);
+                                const bool ok = sp < np;
+                                ls[u] = ok ? __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r) : -INFINITY;
+                                v[u] = ok ? __ldcg(reinterpret_cast<const float4*>(
+                                               a.part_o + ((size_t)sl * a.hc_rows + r) * D + c4 * 4))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const float wgt = (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - M) * kLog2e) * inv;
+                                acc.x = fmaf(wgt, v[u].x, acc.x);
+                                acc.y = fmaf(wgt, v[u].y, acc.y);
+                                acc.z = fmaf(wgt, v[u].z, acc.z);
+                                acc.w = fmaf(wgt, v[u].w, acc.w);
+                            }
                         }
                         const size_t off = ((size_t)cur.b * a.H + h0 + r) * D + c4 * 4;
                         if (a.out_bf16) {

@@ -21,7 +21,7 @@ Sources (the pages this library follows), cited by page title and section:
 * [CH7] shippingwang.com ch.7 "KV Cache 优化", §7.3 (query head h reads KV
   head h // g; never replicate, check the head axis).
 
-Readings where the pages are silent (listed again in the design doc):
+Readings where the pages are silent:
 
 * RoPE: the pages state only that R_m depends on the position m and that
   R_m^T R_n = R_{n-m} ([ARG] §四.4); the frequencies are deferred to another
@@ -218,13 +218,12 @@ def gqa_decode(q, k, v, seqlens, scale=None, block_table=None, window=0):
     lse = np.zeros((B, h))
     for b in range(B):
         slots = window_slots(int(seqlens[b]), window)
-        for hh in range(h):
-            kv = hh // g
+        for kv in range(n_kv):
+            # the query heads hh with hh // g == kv share this KV head's rows
+            heads = slice(kv * g, (kv + 1) * g)
             K = gather_slots(k, b, slots, block_table, kv)
             V = gather_slots(v, b, slots, block_table, kv)
-            o, l = attend(q[b, hh:hh + 1], K, V, scale)
-            out[b, hh] = o[0]
-            lse[b, hh] = l[0]
+            out[b, heads], lse[b, heads] = attend(q[b, heads], K, V, scale)
     return out, lse
 
 
@@ -330,8 +329,12 @@ def mla_prefill(q_nope, q_rope, k_nope, k_rope, v, scale=None, kv_offset=None):
 
 
 # ----------------------------------------------------------------------------
-# flash-decoding split and merge ([ARG] §五.2, last paragraph: split the KV
-# along the sequence, softmax each piece locally, then merge the normalisers)
+# MLA absorption projections on either side of the absorbed decode ([ARG]
+# §四.5; [MLA] §4): W_UK folded into the query, W_UV applied to the latent
+# output
+# ----------------------------------------------------------------------------
+
+
 def mla_absorb_q(q_nope, W_UK):
     """Query-side absorption ([ARG] "attention-variants-and-kv-cache" §四.5;
     [MLA] "multi-head-latent-attention" §4): q~_{b,h} = W_UK,h^T q^C_{b,h},
@@ -357,6 +360,9 @@ def mla_project_out(lat, W_UV):
     return out
 
 
+# ----------------------------------------------------------------------------
+# flash-decoding split and merge ([ARG] §五.2, last paragraph: split the KV
+# along the sequence, softmax each piece locally, then merge the normalisers)
 # ----------------------------------------------------------------------------
 
 

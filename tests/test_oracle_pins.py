@@ -118,12 +118,15 @@ def test_repeat_kv_equals_mha():
     kr = np.repeat(k, h // n_kv, axis=1)
     vr = np.repeat(v, h // n_kv, axis=1)
     o2, l2 = oracle.gqa_decode(q, kr, vr, sl)
-    np.testing.assert_array_equal(o1, o2)
-    np.testing.assert_array_equal(l1, l2)
+    # equal up to fp64 rounding order (a group's heads share one product);
+    # a head read from the wrong KV head differs by O(1)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
     # MQA is the g = h end of the same family
     o3, _ = oracle.gqa_decode(q, k[:, :1], v[:, :1], sl)
     o4, _ = oracle.gqa_decode(q, np.repeat(k[:, :1], h, 1), np.repeat(v[:, :1], h, 1), sl)
-    np.testing.assert_array_equal(o3, o4)
+    np.testing.assert_allclose(o3, o4, rtol=0, atol=1e-12)
+    assert np.abs(o1[:, 0] - o1[:, h // n_kv]).max() > 0.1     # the groups do differ
 
 
 def test_head_axis_detector():
@@ -617,40 +620,44 @@ def test_window_append_ring_keeps_last_w():
 
 def test_closed_forms_match_printed_values():
     g = {k: v[0] for k, v in read_golden("cache_sizes.txt").items()}
-    mla = cf.kv_elems_per_token_per_layer("mla", d_c=512, d_rope=64)
+    per_layer_values = lambda heads, d: cf.kv_cache_bytes_per_token(1, heads, d, elem_bytes=1)
+    mla = cf.mla_latent_values_per_token(512, 64)
     assert mla == g["mla_elems_per_token_per_layer"]
     assert 64 / 512 == g["mla_rope_overhead"]
-    mha5120 = cf.kv_elems_per_token_per_layer("mha", n_heads=40, head_dim=128)
+    mha5120 = per_layer_values(40, 128)               # 2 * d_model at d_model = 5120
+    assert mha5120 == 10240
     assert round(mha5120 / mla, 1) == g["mha_vs_mla_ratio_dmodel5120"]
-    assert mha5120 / 512 == g["mha_vs_pure_mla_ratio_dmodel5120"]
-    assert cf.kv_bytes_per_token(60, mla) == g["mla_60_layer_bytes_per_token"]
-    assert cf.kv_bytes_per_token(60, mla) / 1024 == 67.5
-    assert cf.kv_elems_per_token_per_layer("mha", n_heads=32, head_dim=128) == g["llama2_mha_elems"]
-    assert cf.kv_elems_per_token_per_layer("gqa", n_kv_heads=8, head_dim=128) == g["llama2_gqa8_elems"]
-    assert cf.kv_elems_per_token_per_layer("mqa", head_dim=128) == g["llama2_mqa_elems"]
-    assert cf.kv_elems_per_token_per_layer("mla", d_c=512) == g["llama2_mla_elems"]
-    l8 = cf.kv_elems_per_token_per_layer("gqa", n_kv_heads=8, head_dim=128)
-    assert cf.kv_bytes_per_token(32, l8) == g["llama3_8b_gqa_bytes_per_token"]
-    l8m = cf.kv_elems_per_token_per_layer("mha", n_heads=32, head_dim=128)
-    assert cf.kv_bytes_per_token(32, l8m) == g["llama3_8b_mha_bytes_per_token"]
-    assert cf.kv_bytes_per_token(80, l8) == g["llama3_70b_gqa_bytes_per_token"]
-    v3 = cf.kv_bytes_per_token(61, mla)
+    assert mha5120 / cf.mla_latent_values_per_token(512, 0) == g["mha_vs_pure_mla_ratio_dmodel5120"]
+    assert cf.mla_cache_bytes_per_token(60) == g["mla_60_layer_bytes_per_token"]
+    assert cf.mla_cache_bytes_per_token(60) / 1024 == 67.5
+    assert per_layer_values(32, 128) == g["llama2_mha_elems"]
+    assert per_layer_values(8, 128) == g["llama2_gqa8_elems"]
+    assert per_layer_values(1, 128) == g["llama2_mqa_elems"]
+    assert cf.mla_latent_values_per_token(512, 0) == g["llama2_mla_elems"]
+    assert cf.kv_cache_bytes_per_token(32, 8, 128) == g["llama3_8b_gqa_bytes_per_token"]
+    assert cf.kv_cache_bytes_per_token(32, 32, 128) == g["llama3_8b_mha_bytes_per_token"]
+    assert cf.kv_cache_bytes_per_token(80, 8, 128) == g["llama3_70b_gqa_bytes_per_token"]
+    v3 = cf.mla_cache_bytes_per_token(61)
     assert v3 == g["deepseek_v3_mla_bytes_per_token"]
-    v3m = cf.kv_bytes_per_token(61, cf.kv_elems_per_token_per_layer("mha", n_heads=128, head_dim=128))
+    v3m = cf.kv_cache_bytes_per_token(61, 128, 128)
     assert v3m == g["deepseek_v3_as_mha_bytes_per_token"]
     assert round(v3m / v3, 1) == g["deepseek_v3_mha_over_mla"]
     gib = 1024 ** 3
-    assert round(131072 * 131072 / gib, 1) == g["llama3_8b_128k_gib"]
-    assert round(327680 * 131072 / gib, 1) == g["llama3_70b_128k_gib"]
+    assert round(cf.kv_cache_bytes_per_token(32, 8, 128) * 131072 / gib, 1) == g["llama3_8b_128k_gib"]
+    assert round(cf.kv_cache_bytes_per_token(80, 8, 128) * 131072 / gib, 1) == g["llama3_70b_128k_gib"]
     assert round(v3 * 131072 / gib, 1) == g["deepseek_v3_128k_gib"]
-    assert cf.decode_intensity("mha", 32, l8m, head_dim=128) == g["intensity_mha"]
-    assert cf.decode_intensity("gqa", 32, l8, head_dim=128) == g["intensity_llama3_8b"]
-    assert cf.decode_intensity("gqa", 64, l8, head_dim=128) == g["intensity_llama3_70b"]
-    assert round(cf.decode_intensity("mla", 128, mla, d_c=512, d_rope=64)) == g["intensity_deepseek_v3"]
-    assert cf.mla_flops_per_token(128) == g["mla_flops_per_token_per_layer"]
-    assert mla * 2 == g["mla_bytes_per_token_per_layer"]
-    assert l8 * 2 == g["llama3_8b_gqa_bytes_per_token_per_layer"]
-    assert 32 * 2 * 256 == g["llama3_8b_gqa_flops_per_token_per_layer"]
+    assert cf.grouped_decode_intensity(1) == g["intensity_mha"]
+    assert cf.grouped_decode_intensity(32 // 8) == g["intensity_llama3_8b"]
+    assert cf.grouped_decode_intensity(64 // 8) == g["intensity_llama3_70b"]
+    assert round(cf.mla_decode_intensity(128)) == g["intensity_deepseek_v3"]
+    assert cf.mla_decode_flops_per_token(128) == g["mla_flops_per_token_per_layer"]
+    assert cf.mla_cache_bytes_per_token(1) == g["mla_bytes_per_token_per_layer"]
+    assert cf.kv_cache_bytes_per_token(1, 8, 128) == g["llama3_8b_gqa_bytes_per_token_per_layer"]
+    # [ARG] §四.6 prints the Llama-3-8B GQA FLOPs per cached token per layer:
+    # 32 heads, a 128-long dot and a 128-long weighted sum each
+    assert 32 * 2 * (128 + 128) == g["llama3_8b_gqa_flops_per_token_per_layer"]
+    assert (g["llama3_8b_gqa_flops_per_token_per_layer"] / g["llama3_8b_gqa_bytes_per_token_per_layer"]
+            == cf.grouped_decode_intensity(4))
     assert 192 + 128 == g["dot_len_unabsorbed"] and 576 + 512 == g["dot_len_absorbed"]
     assert round(cf.mla_vs_mha_read_ratio(20), 2) == g["mla_mha_read_ratio_s20"]
     assert abs(cf.mla_vs_mha_read_ratio(1e12) - g["mla_mha_read_ratio_limit"]) < 1e-9

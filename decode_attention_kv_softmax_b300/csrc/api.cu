@@ -192,14 +192,12 @@ struct MlaPlan {
     size_t off_lse, off_o, bytes;
 };
 
-constexpr int kMaxBatchMla = 2048;
-
 kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
     if (!p) return fail(KVDEC_ERR_INVALID_ARG, "params is NULL");
     if (p->num_heads != 128)
         return fail(KVDEC_ERR_UNSUPPORTED, "num_heads %d (the MLA kernel is built for 128)", p->num_heads);
-    if (p->batch < 1 || p->batch > kMaxBatchMla)
-        return fail(KVDEC_ERR_INVALID_ARG, "batch %d outside [1, %d]", p->batch, kMaxBatchMla);
+    if (p->batch < 1 || p->batch > kvdec::max_batch_mla())
+        return fail(KVDEC_ERR_INVALID_ARG, "batch %d outside [1, %d]", p->batch, kvdec::max_batch_mla());
     if (p->num_pages < 1 || p->max_blocks < 1)
         return fail(KVDEC_ERR_INVALID_ARG, "num_pages and max_blocks must be >= 1");
     DeviceInfo di;
@@ -237,6 +235,8 @@ void set_last_error(const char* msg) { g_last_error = msg; }
 extern "C" {
 
 int kvdec_abi_version(void) { return KVDEC_ABI_VERSION; }
+
+int32_t kvdec_mla_max_batch(void) { return kvdec::max_batch_mla(); }
 
 int64_t kvdec_params_size(int kind) {
     switch (kind) {

@@ -245,27 +245,6 @@ KVDEC_DEVINL void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_
         : "memory");
 }
 
-// Tensor-map loads multicast to the CTAs of the cluster in `mask`: the box
-// lands at the same shared-memory offset in each, and each one's mbarrier
-// at `bar`'s offset counts the bytes.
-KVDEC_DEVINL void tma_load_3d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1, int c2,
-                                 uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4, %5}], [%2], %6, %7;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask), "l"(policy)
-        : "memory");
-}
-
-KVDEC_DEVINL void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                 uint16_t mask, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
-        : "memory");
-}
-
 // Bring a tensor-map box into L2 ahead of its load (no shared memory, no
 // barrier; boxes past the tensor's edge are ignored).
 KVDEC_DEVINL void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {

@@ -138,6 +138,7 @@ struct MlaExpandArgs {
 };
 cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs& a, cudaStream_t st);
 int max_pairs_mla(int B);
+int max_batch_mla();   // largest batch whose tile table fits in shared memory
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st);

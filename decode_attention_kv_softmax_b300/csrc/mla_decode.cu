@@ -755,9 +755,14 @@ int optin_smem() {
 // long-context run with them faulted the GPU; the cause is not found, so
 // that configuration is not built.
 static_assert(KVDEC_MLA_PB == 1, "the two-P-buffer configuration is not built");
-// the preferred configuration when it fits beside the batch's tile table,
-// else four stages and one P buffer
-bool preferred(int B) { return mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB>::smem_bytes(B) <= optin_smem(); }
+using Built = mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB>;
+// The per-sequence tile table shares the CTA's shared memory with the cache
+// stages, so the batch is bounded by what is left of the 227 KB a CTA of
+// sm_100 / sm_103 may opt in to.  No other stage count is built.
+constexpr int kOptinSmem = 227 * 1024;
+constexpr int kMaxBatch = (kOptinSmem - Built::smem_bytes(0)) / 4;
+static_assert(kMaxBatch >= 256, "the five-stage layout leaves room for at least 256 sequences");
+bool fits(int B) { return B <= kMaxBatch && Built::smem_bytes(B) <= optin_smem(); }
 
 template <int NS, int PB>
 cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
@@ -794,9 +799,12 @@ int max_pairs_ns(int B) {
 }  // namespace
 
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    return preferred(a.B) ? launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(maps, a, pairs, st) : launch_ns<4, 1>(maps, a, pairs, st);
+    if (!fits(a.B)) return cudaErrorInvalidValue;   // the host checks kMaxBatch first
+    return launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(maps, a, pairs, st);
 }
 
-int max_pairs_mla(int B) { return preferred(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(B) : max_pairs_ns<4, 1>(B); }
+int max_pairs_mla(int B) { return fits(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(B) : 0; }
+
+int max_batch_mla() { return kMaxBatch; }
 
 }  // namespace kvdec

@@ -4,15 +4,12 @@
 // and 128; [ARG] §五.2: FlashAttention's tiled online softmax; §五.3: causal
 // mask).
 //
-// CTA = one head and 128 query rows, 8 warps.  A cluster pairs the CTAs of
-// two adjacent query blocks of a head, which read the same K/V tiles:
+// CTA = one head and 128 query rows, 8 warps; the CTAs are independent (the
+// query blocks of a head read the same K/V tiles, which L2 serves again):
 //   warp 0  TMA producer of Q (3 boxes of 128 rows x 64 dims) and, per
 //           128-key tile, K (k_nope 0-63, 64-127, k_rope) into a 2-stage ring;
-//   warp 6  TMA producer of V (2 boxes of 64 dims) into a 2-stage ring.
-//           For a tile both CTAs need, each loads 64 of its 128 token rows
-//           and multicasts them to both, so L2 serves each tile once per
-//           pair; a stage refills once both CTAs have released it.  A tile
-//           only one CTA needs (the later block's diagonal) it loads alone;
+//   warp 6  TMA producer of V (2 boxes of 64 dims) into a 2-stage ring;
+//           a stage refills once this CTA's MMAs have released it;
 //   warp 1  owns TMEM and issues S(j) = Q K_j^T into S buffer j mod 2 (12
 //           MMAs of M=128, N=128, K=16; the K stage is released when they
 //           complete);
@@ -69,31 +66,27 @@ constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0, kTmemO = 256, kTmemP = 384;
 
-// key tiles of query block qb (0 for the idle partner of an odd count)
+// key tiles of query block qb (the causal triangle up to its last row)
 __device__ __forceinline__ int block_tiles(const MlaPrefillArgs& a, int qb) {
-    if (qb < 0) return 0;
     const int q0 = qb * kBM;
     const int kend = min(a.s_kv, a.kv_offset + min(q0 + kBM, a.s_q));
     return (kend + kBN - 1) / kBN;
 }
 }  // namespace pft
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
+__global__ void __launch_bounds__(pft::kThreads, 1)
     mla_prefill_tc_kernel(const __grid_constant__ MlaPrefillMaps maps, const MlaPrefillArgs a) {
     using namespace pft;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t rank = cluster_ctarank();
-    // heaviest query blocks first; an odd count leaves the last CTA idle
+    // heaviest query blocks first
     const int G = (a.s_q + kBM - 1) / kBM;
     const int qb = G - 1 - (int)blockIdx.x;
     const int hh = blockIdx.y;
     const int q0 = qb * kBM;
     const int nt = block_tiles(a, qb);
-    const int shared = min(nt, block_tiles(a, G - 1 - (int)(blockIdx.x ^ 1u)));   // tiles of both CTAs
-    constexpr uint16_t kBoth = 0x3;
 
     const uint32_t bar0 = smem_addr(smem + kOffBars);
     auto bar = [bar0](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -111,15 +104,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
         }
         mbar_init(bar(B_ODONE), 1);
         mbar_init(bar(B_DONE), 1);
-        // a stage is released by both CTAs of the pair (a tile only this CTA
-        // reads is released twice by it)
         for (int s = 0; s < kNK; ++s) {
             mbar_init(bar(B_KFULL + s), 1);
-            mbar_init(bar(B_KEMPTY + s), 2);
+            mbar_init(bar(B_KEMPTY + s), 1);
         }
         for (int s = 0; s < kNV; ++s) {
             mbar_init(bar(B_VFULL + s), 1);
-            mbar_init(bar(B_VEMPTY + s), 2);
+            mbar_init(bar(B_VEMPTY + s), 1);
         }
         misc[1] = 0;
         fence_barrier_init();
@@ -131,7 +122,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
     }
     __syncthreads();
     tc_fence_after();
-    cluster_sync_all();                                    // the peer's barriers exist
     const uint32_t tmem = (uint32_t)misc[0];
 
     if (nt > 0 && (warp == 0 || warp == 6)) {
@@ -159,53 +149,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
             for (int j = 0; j < nt; ++j) {
                 const int k0 = j * kBN, st = j % NS;
                 const uint32_t ep = (uint32_t)(((j / NS) & 1) ^ 1);
-                if (!mbar_try_wait_acq_cluster(bar(empty0 + st), ep) &&
-                    !wait_cluster_or_abort(bar(empty0 + st), ep, abort_word, a.err, a.timeout_ns))
-                    break;
+                if (!wait_or_abort(bar(empty0 + st), ep, abort_word, a.err, a.timeout_ns)) break;
                 const uint32_t fb = bar(full0 + st), dst = ring + st * stage_bytes;
                 mbar_arrive_expect_tx(fb, stage_bytes);
-                if (j < shared) {
-                    // this CTA's half of the token rows, to both CTAs
-                    const uint32_t d = dst + rank * kHalf;
-                    const int t = k0 + 64 * (int)rank;
-                    if (is_k) {
-                        tma_load_3d_mc(d, &maps.kn, fb, 0, hh, t, kBoth, keep);
-                        tma_load_3d_mc(d + kBox, &maps.kn, fb, 64, hh, t, kBoth, keep);
-                        tma_load_2d_mc(d + 2 * kBox, &maps.kr, fb, 0, t, kBoth, keep);
-                    } else {
-                        tma_load_3d_mc(d, &maps.v, fb, 0, hh, t, kBoth, keep);
-                        tma_load_3d_mc(d + kBox, &maps.v, fb, 64, hh, t, kBoth, keep);
-                    }
-                } else {
+                // the tile's 128 token rows as two 64-row boxes per dim block
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t d = dst + h * kHalf;
-                        const int t = k0 + 64 * h;
-                        if (is_k) {
-                            tma_load_3d_hint(d, &maps.kn, fb, 0, hh, t, keep);
-                            tma_load_3d_hint(d + kBox, &maps.kn, fb, 64, hh, t, keep);
-                            tma_load_2d(d + 2 * kBox, &maps.kr, fb, 0, t, keep);
-                        } else {
-                            tma_load_3d_hint(d, &maps.v, fb, 0, hh, t, keep);
-                            tma_load_3d_hint(d + kBox, &maps.v, fb, 64, hh, t, keep);
-                        }
+                for (int h = 0; h < 2; ++h) {
+                    const uint32_t d = dst + h * kHalf;
+                    const int t = k0 + 64 * h;
+                    if (is_k) {
+                        tma_load_3d_hint(d, &maps.kn, fb, 0, hh, t, keep);
+                        tma_load_3d_hint(d + kBox, &maps.kn, fb, 64, hh, t, keep);
+                        tma_load_2d(d + 2 * kBox, &maps.kr, fb, 0, t, keep);
+                    } else {
+                        tma_load_3d_hint(d, &maps.v, fb, 0, hh, t, keep);
+                        tma_load_3d_hint(d + kBox, &maps.v, fb, 64, hh, t, keep);
                     }
                 }
                 ++issued;
             }
-            // never leave TMA writes in flight (the peer's halves included)
+            // never leave TMA writes in flight
             if (is_k && !mbar_wait_bounded(bar(B_Q), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
             for (int i = (issued > NS ? issued - NS : 0); i < issued; ++i)
                 if (!mbar_wait_bounded(bar(full0 + i % NS), (uint32_t)((i / NS) & 1), a.timeout_ns)) {
                     report(a.err, KVDEC_DEVERR_TIMEOUT);
                     break;
                 }
-            // the peer's last releases of shared tiles have landed here (the
-            // earlier ones were waited for before refilling their stages)
-            for (int i = max(0, nt - NS); i < shared; ++i)
-                if (!wait_cluster_or_abort(bar(empty0 + i % NS), (uint32_t)((i / NS) & 1), abort_word, a.err,
-                                           a.timeout_ns))
-                    break;
         }
     } else if (nt > 0 && (warp == 1 || warp == 7)) {
         // ------------------------------------------------------- MMA issuers
@@ -219,15 +188,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
             int ok = 1;
             if (lane == 0) ok = wait_or_abort(b, par, abort_word, a.err, a.timeout_ns) ? 1 : 0;
             return __all_sync(0xffffffffu, ok) != 0;
-        };
-        // release a ring stage: to both CTAs for a shared tile, else twice here
-        auto release = [&](uint32_t b, int j) {
-            if (j < shared) {
-                umma_commit_mc_w(b, kBoth);
-            } else {
-                umma_commit_w(b);
-                umma_commit_w(b);
-            }
         };
         if (warp == 1) {
             constexpr uint32_t iS = umma_idesc_bf16(128, 128, false, false);
@@ -246,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
                                    dQ + (uint64_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4),
                                    dk + (uint64_t)(((ks >> 2) * kBox + (ks & 3) * 32) >> 4), iS, ks > 0 ? 1u : 0u);
                 umma_commit_w(bar(B_SFULL + sb));
-                release(bar(B_KEMPTY + ks_), j);
+                umma_commit_w(bar(B_KEMPTY + ks_));   // the K stage may refill
             }
             // every MMA of this warp has completed before TMEM is freed
             umma_commit_w(bar(B_DONE));
@@ -265,7 +225,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
                     umma_bf16_ts_w(tmem + kTmemO, tmem + kTmemP + 64u * pb + 8u * ks,
                                    dv + (uint64_t)((ks * 2048) >> 4), iP, (j > 0 || ks > 0) ? 1u : 0u);
                 umma_commit_w(bar(B_PFREE + pb));
-                release(bar(B_VEMPTY + vs), j);
+                umma_commit_w(bar(B_VEMPTY + vs));    // the V stage may refill
             }
             // O is final (or the loop was abandoned) once every PV has completed
             umma_commit_w(bar(B_ODONE));
@@ -397,8 +357,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-    cluster_sync_all();   // the peer no longer touches this CTA's shared memory
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
@@ -406,9 +364,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(pft::kThreads, 1)
 }
 
 cudaError_t launch_mla_prefill_tc(const MlaPrefillMaps& maps, const MlaPrefillArgs& a, cudaStream_t st) {
-    // query blocks in pairs (cluster of two); an odd count gets an idle partner
     const int G = (a.s_q + pft::kBM - 1) / pft::kBM;
-    const dim3 grid((G + 1) & ~1, a.num_heads);
+    const dim3 grid(G, a.num_heads);
     cudaError_t e = cudaFuncSetAttribute(mla_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          pft::kSmem);
     if (e != cudaSuccess) return e;

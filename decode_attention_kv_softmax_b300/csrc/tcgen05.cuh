@@ -132,16 +132,6 @@ KVDEC_DEVINL void umma_commit_w(uint32_t mbar) {
         : "memory");
 }
 
-// Warp-wide commit that arrives on the mbarrier at `mbar`'s offset in each
-// CTA of the cluster named in `mask`.
-KVDEC_DEVINL void umma_commit_mc_w(uint32_t mbar, uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(mbar),
-        "h"(mask)
-        : "memory");
-}
-
 // Warp-collective load / store of 32 32-bit columns per lane.
 KVDEC_DEVINL void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     asm volatile(

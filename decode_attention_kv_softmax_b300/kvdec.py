@@ -7,7 +7,6 @@ fallback: if libkvdec.so is missing or a call fails, these functions raise.
 from __future__ import annotations
 
 import ctypes
-import math
 import os
 import threading
 from ctypes import c_float, c_int32, c_int64, c_size_t, c_uint64, c_void_p
@@ -87,7 +86,7 @@ EXPORTS = ["kvdec_abi_version", "kvdec_params_size", "kvdec_status_string",
            "kvdec_mla_workspace_bytes", "kvdec_mla_decode_absorbed", "kvdec_append_rope",
            "kvdec_combine_splits", "kvdec_selftest_wait_timeout",
            "kvdec_gqa_decode_noalloc", "kvdec_mla_absorb_q", "kvdec_mla_project_out",
-           "kvdec_mla_prefill_expand", "kvdec_mla_prefill"]
+           "kvdec_mla_prefill_expand", "kvdec_mla_prefill", "kvdec_mla_max_batch"]
 
 _lib = None
 _lock = threading.Lock()
@@ -105,6 +104,7 @@ def load(path: str = LIB_PATH):
                 "`python -m decode_attention_kv_softmax_b300.build` (no CPU fallback)")
         lib = ctypes.CDLL(path)
         lib.kvdec_abi_version.restype = ctypes.c_int
+        lib.kvdec_mla_max_batch.restype = ctypes.c_int32
         lib.kvdec_params_size.restype = c_int64
         lib.kvdec_params_size.argtypes = [ctypes.c_int]
         lib.kvdec_status_string.restype = ctypes.c_char_p
@@ -502,10 +502,6 @@ def selftest_wait_timeout(timeout_ns: int, error_flag, stream=None):
     lib = load()
     _check(lib.kvdec_selftest_wait_timeout(timeout_ns, _ptr(error_flag), _stream(stream)),
            "kvdec_selftest_wait_timeout")
-
-
-def default_scale_gqa(d: int) -> float:
-    return 1.0 / math.sqrt(d)
 
 
 # ---------------------------------------------------------------- MLA prefill (non-absorbed)

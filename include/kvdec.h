@@ -192,7 +192,10 @@ kvdec_status kvdec_gqa_decode_noalloc(const kvdec_gqa_params* p, void* stream);
  *   cache bf16 [num_pages, 64, 576]; block_table int32 [batch, max_blocks]
  *   seqlens int32 [batch]; out [batch, num_heads, 512] F32 or BF16;
  *   lse fp32 [batch, num_heads] or NULL
- * Supported: num_heads == 128 (tensor-core tile height).
+ * Supported: num_heads == 128 (tensor-core tile height) and
+ * batch <= kvdec_mla_max_batch(): the kernel keeps a per-sequence tile table
+ * in shared memory beside its cache stages, so a larger batch is rejected
+ * with KVDEC_ERR_INVALID_ARG before any launch (split it into calls).
  * Workspace: as for kvdec_gqa_decode (no initialisation needed).
  */
 typedef struct kvdec_mla_params {
@@ -218,6 +221,9 @@ typedef struct kvdec_mla_params {
 
 size_t kvdec_mla_workspace_bytes(const kvdec_mla_params* p);
 kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream);
+/* Largest batch one kvdec_mla_decode_absorbed call accepts (a build
+ * constant; makes no CUDA call). */
+int32_t kvdec_mla_max_batch(void);
 
 /* ------------------------------------------------------------------------ */
 /* Cache append with RoPE                                                    */

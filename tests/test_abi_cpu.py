@@ -140,3 +140,21 @@ def test_prefill_argument_checks(lib):
     e.c_kv, e.w_uk, e.w_uv, e.k_nope, e.v = 256, 512, 768, 1024, 1280
     e.s, e.num_heads = 0, 128
     assert lib.kvdec_mla_prefill_expand(ctypes.byref(e), None) == 1
+
+
+def test_mla_batch_limit(lib):
+    """The MLA decode keeps a tile table of batch + 1 ints in shared memory
+    beside five 36 KB cache stages; the largest batch that fits in the
+    227 KB a CTA may use is the limit, and one more sequence is rejected on
+    the host (INVALID_ARG) before any device query."""
+    limit = lib.kvdec_mla_max_batch()
+    assert limit == 411
+    m = kvdec.MlaParams()
+    m.num_heads, m.num_pages, m.max_blocks = 128, 4, 4
+    m.batch = limit + 1
+    assert lib.kvdec_mla_decode_absorbed(ctypes.byref(m), None) == 1
+    assert f"outside [1, {limit}]" in lib.kvdec_last_error().decode()
+    assert lib.kvdec_mla_workspace_bytes(ctypes.byref(m)) == 0
+    m.batch = limit                  # passes the batch check; no device here
+    st = lib.kvdec_mla_decode_absorbed(ctypes.byref(m), None)
+    assert st != 1 or "batch" not in lib.kvdec_last_error().decode()

@@ -52,7 +52,33 @@ std::map<std::tuple<int, int, int, int, int>, int> g_occupancy;  // (dev, kind, 
 
 bool device_info(DeviceInfo& out, int& dev) {
     if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    // per-thread memo first: the common case takes no lock
+    constexpr int kMemo = 8;
+    thread_local int memo_dev[kMemo];
+    thread_local DeviceInfo memo_info[kMemo];
+    thread_local int memo_n = 0;
+    for (int i = 0; i < memo_n; ++i)
+        if (memo_dev[i] == dev) {
+            out = memo_info[i];
+            return true;
+        }
     std::lock_guard<std::mutex> lk(g_mu);
+    if (memo_n < kMemo) {
+        auto it = g_devices.find(dev);
+        DeviceInfo d;
+        if (it != g_devices.end()) {
+            d = it->second;
+        } else {
+            if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+                return false;
+            g_devices[dev] = d;
+        }
+        memo_dev[memo_n] = dev;
+        memo_info[memo_n] = d;
+        ++memo_n;
+        out = d;
+        return true;
+    }
     auto it = g_devices.find(dev);
     if (it != g_devices.end()) {
         out = it->second;
@@ -64,6 +90,34 @@ bool device_info(DeviceInfo& out, int& dev) {
     g_devices[dev] = d;
     out = d;
     return true;
+}
+
+// Resident CTAs (or CTA pairs) per launch shape, keyed (device, kind, D, MT,
+// batch): a per-thread memo in front of the process-wide map.
+using OccKey = std::tuple<int, int, int, int, int>;
+template <typename F>
+int cached_occupancy(const OccKey& key, F&& query) {
+    constexpr int kMemo = 16;
+    thread_local OccKey memo_key[kMemo];
+    thread_local int memo_val[kMemo];
+    thread_local int memo_n = 0, memo_next = 0;
+    for (int i = 0; i < memo_n; ++i)
+        if (memo_key[i] == key) return memo_val[i];
+    int v;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occupancy.find(key);
+        if (it == g_occupancy.end()) {
+            v = query();
+            g_occupancy[key] = v;
+        } else {
+            v = it->second;
+        }
+    }
+    const int slot = memo_n < kMemo ? memo_n++ : (memo_next++ % kMemo);
+    memo_key[slot] = key;
+    memo_val[slot] = v;
+    return v;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -80,12 +134,45 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
+// Per-thread memo of encoded 2-D tensor maps.  An encoded map is a pure
+// function of its encode arguments, so a hit returns the bytes the driver
+// would produce again; a decode loop that passes the same buffers every step
+// encodes each of its maps once per thread.
+struct MapKey {
+    const void* base;
+    uint64_t rows, cols, stride;
+    uint32_t box_cols, box_rows;
+    int32_t swz, dt;
+};
+struct MapMemo {
+    MapKey key;
+    CUtensorMap map;
+};
+constexpr int kMapMemo = 32;
+thread_local MapMemo t_maps[kMapMemo];
+thread_local int t_maps_n = 0, t_maps_next = 0;
+
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, box of
 // box_cols x box_rows elements, given swizzle.
 kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                        uint64_t row_stride_bytes, uint32_t box_cols, uint32_t box_rows,
                        CUtensorMapSwizzle swz,
                        CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
+    MapKey key;
+    memset(&key, 0, sizeof(key));
+    key.base = base;
+    key.rows = rows;
+    key.cols = cols;
+    key.stride = row_stride_bytes;
+    key.box_cols = box_cols;
+    key.box_rows = box_rows;
+    key.swz = (int32_t)swz;
+    key.dt = (int32_t)dt;
+    for (int i = 0; i < t_maps_n; ++i)
+        if (memcmp(&t_maps[i].key, &key, sizeof(key)) == 0) {
+            *map = t_maps[i].map;
+            return KVDEC_OK;
+        }
     auto enc = tensor_map_encoder();
     if (!enc) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
     const cuuint64_t dims[2] = {cols, rows};
@@ -96,6 +183,9 @@ kvdec_status encode_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(KVDEC_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    MapMemo& slot = t_maps[t_maps_n < kMapMemo ? t_maps_n++ : (t_maps_next++ % kMapMemo)];
+    slot.key = key;
+    slot.map = *map;
     return KVDEC_OK;
 }
 
@@ -158,18 +248,8 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     DeviceInfo di;
     int dev;
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
-    int occ;
-    {
-        auto key = std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch);
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_occupancy.find(key);
-        if (it == g_occupancy.end()) {
-            occ = kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, p->batch);
-            g_occupancy[key] = occ;
-        } else {
-            occ = it->second;
-        }
-    }
+    const int occ = cached_occupancy(std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch),
+                                     [&] { return kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, p->batch); });
     if (occ < 1) return fail(KVDEC_ERR_CUDA, "GQA kernel does not fit on this device");
     pl.grid = di.sm_count * occ;
     // max_ctas > 0 sets the number of work items (CTAs); above one resident
@@ -203,18 +283,8 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
     DeviceInfo di;
     int dev;
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
-    int pairs;
-    {
-        auto key = std::make_tuple(dev, 1, 0, 0, p->batch);
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_occupancy.find(key);
-        if (it == g_occupancy.end()) {
-            pairs = kvdec::max_pairs_mla(p->batch);
-            g_occupancy[key] = pairs;
-        } else {
-            pairs = it->second;
-        }
-    }
+    int pairs = cached_occupancy(std::make_tuple(dev, 1, 0, 0, p->batch),
+                                 [&] { return kvdec::max_pairs_mla(p->batch); });
     if (pairs < 1) return fail(KVDEC_ERR_CUDA, "MLA kernel clusters do not fit on this device");
     if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
     pl.pairs = pairs;

@@ -573,7 +573,7 @@ static cudaError_t launch_gqa_t(const CUtensorMap& tk, const CUtensorMap& tv, co
     using L = GqaSmem<D, MT, NS, F8>;
     const int smem = L::bytes(a.B);
     auto kern = gqa_decode_kernel<D, MT, NS, F8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(kern));
     if (e != cudaSuccess) return e;
     kern<<<grid, 160, smem, st>>>(tk, tv, a);
     return cudaGetLastError();
@@ -584,8 +584,7 @@ static int occupancy_gqa_t(int B) {
     using L = GqaSmem<D, MT, NS, F8>;
     const int smem = L::bytes(B);
     auto kern = gqa_decode_kernel<D, MT, NS, F8>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return 0;
+    if (allow_max_dynamic_smem(reinterpret_cast<const void*>(kern)) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 160, smem) != cudaSuccess) return 0;
     return n;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "launch_cache.h"
 
 namespace kvdec {
 

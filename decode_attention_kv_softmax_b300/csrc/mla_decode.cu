@@ -767,7 +767,7 @@ bool fits(int B) { return B <= kMaxBatch && Built::smem_bytes(B) <= optin_smem()
 template <int NS, int PB>
 cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
     const int smem = mla::Layout<NS, PB>::smem_bytes(a.B);
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<NS, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB>));
     if (e != cudaSuccess) return e;
     mla_decode_kernel<NS, PB><<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
     return cudaGetLastError();
@@ -776,8 +776,7 @@ cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStre
 template <int NS, int PB>
 int max_pairs_ns(int B) {
     const int smem = mla::Layout<NS, PB>::smem_bytes(B);
-    if (cudaFuncSetAttribute(mla_decode_kernel<NS, PB>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-        return 0;
+    if (allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB>)) != cudaSuccess) return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

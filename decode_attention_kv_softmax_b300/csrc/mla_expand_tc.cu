@@ -149,8 +149,7 @@ __global__ void __launch_bounds__(192, 2)
 
 cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs& a, cudaStream_t st) {
     const dim3 grid(a.N / ext::kBN, (a.s + ext::kBM - 1) / ext::kBM, 2);
-    cudaError_t e = cudaFuncSetAttribute(mla_expand_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         ext::kSmem);
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_expand_tc_kernel));
     if (e != cudaSuccess) return e;
     mla_expand_tc_kernel<<<grid, 192, ext::kSmem, st>>>(maps, a);
     return cudaGetLastError();

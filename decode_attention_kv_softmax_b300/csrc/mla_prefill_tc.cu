@@ -366,8 +366,7 @@ __global__ void __launch_bounds__(pft::kThreads, 1)
 cudaError_t launch_mla_prefill_tc(const MlaPrefillMaps& maps, const MlaPrefillArgs& a, cudaStream_t st) {
     const int G = (a.s_q + pft::kBM - 1) / pft::kBM;
     const dim3 grid(G, a.num_heads);
-    cudaError_t e = cudaFuncSetAttribute(mla_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         pft::kSmem);
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_prefill_tc_kernel));
     if (e != cudaSuccess) return e;
     mla_prefill_tc_kernel<<<grid, pft::kThreads, pft::kSmem, st>>>(maps, a);
     return cudaGetLastError();

@@ -163,13 +163,11 @@ __global__ void __launch_bounds__(128) mla_proj_kernel(const MlaProjArgs a) {
 cudaError_t launch_mla_proj(bool absorb, const MlaProjArgs& a, cudaStream_t st) {
     const dim3 grid(a.num_heads, (a.batch + proj::kM - 1) / proj::kM, absorb ? 512 / proj::kN : 1);
     if (absorb) {
-        cudaError_t e = cudaFuncSetAttribute(mla_proj_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             proj::smem<true>());
+        cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_proj_kernel<true>));
         if (e != cudaSuccess) return e;
         mla_proj_kernel<true><<<grid, 128, proj::smem<true>(), st>>>(a);
     } else {
-        cudaError_t e = cudaFuncSetAttribute(mla_proj_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             proj::smem<false>());
+        cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_proj_kernel<false>));
         if (e != cudaSuccess) return e;
         mla_proj_kernel<false><<<grid, 128, proj::smem<false>(), st>>>(a);
     }

@@ -15,7 +15,10 @@
 // the moment the library's code is loaded on that GPU until the process
 // exits.  Its device address is looked up once per device, on the first call
 // made with that device current; make that first call before any stream
-// capture on that device.  Every call on a device shares the one array, and
+// capture on that device.  A device reset (cudaDeviceReset) gives the device
+// a new context where the array is loaded again; the next call sees the new
+// context and looks the address up again, so after a reset that call too
+// must come before any capture.  Every call on a device shares the one array, and
 // it keeps whatever the previous call left there.  Nothing in it has to start
 // at zero: the split counters carry a per-call epoch, so a stale word counts
 // as zero.  Calls that overlap on the GPU (two streams, or two host threads)
@@ -32,9 +35,40 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[KVDEC_NOALLOC_S
 
 constexpr int kMaxDevices = 256;
 std::mutex g_scratch_mu;
+// per device: the array's address and the unique id of the context it was
+// looked up in (a reset device gets a new context, where the module and its
+// array are loaded again, possibly at another address)
 void* g_scratch_addr[kMaxDevices];
+unsigned long long g_scratch_ctx[kMaxDevices];
 
-// Device address of the array on the current device (looked up once).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the current context (0 if the driver cannot say).
+unsigned long long current_context_id() {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx && get_id(ctx, &id) == CUDA_SUCCESS)
+        return id;
+    return 0;
+}
+
+// Device address of the array on the current device, looked up once per
+// device (and again if the device's context has changed since).
 kvdec_status scratch_address(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -46,8 +80,11 @@ kvdec_status scratch_address(void** out) {
         kvdec::set_last_error("kvdec_gqa_decode_noalloc: device index out of range");
         return KVDEC_ERR_UNSUPPORTED;
     }
+    // the context id is read before the lookup on later calls and after it on
+    // the first (the lookup itself brings up the device's context)
+    const unsigned long long ctx_now = current_context_id();
     std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
+    if (!g_scratch_addr[dev] || g_scratch_ctx[dev] != ctx_now) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) {
@@ -59,6 +96,7 @@ kvdec_status scratch_address(void** out) {
             return KVDEC_ERR_CUDA;
         }
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = current_context_id();
     }
     *out = g_scratch_addr[dev];
     return KVDEC_OK;

@@ -160,6 +160,9 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream);
  * allocates nothing.
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make it before any stream capture there.
+ *     After a reset of the device (cudaDeviceReset) the next call looks the
+ *     address up again in the new context: make that call before any
+ *     capture too.
  *   - Problems whose scratch would exceed the array are rejected with
  *     KVDEC_ERR_WORKSPACE and a message giving the size needed (lower
  *     max_ctas or batch, or use kvdec_gqa_decode).

@@ -97,6 +97,67 @@ def mla_rows_oracle(case, rows):
     return np.array(outs), np.array(lses)
 
 
+def gqa_full_oracle(case):
+    """Oracle output and lse of a whole GqaCase, one oracle call per
+    (sequence, KV head): the sequence's tokens of that head (its pages, for
+    a paged cache, gathered in logical order) and the g query heads that
+    read it.  Bounded memory at any size: only one head's rows are widened
+    to fp64 at a time.  Handles E4M3 caches (k_scale set) and ring caches
+    (window > 0) through the oracle's own functions."""
+    B, h, d, n_kv = case.B, case.h, case.d, case.n_kv
+    g = h // n_kv
+    sl = case.seqlens.to("cpu").numpy()
+    bt = None if case.block_table is None else case.block_table.to("cpu").numpy()
+    window = getattr(case, "window", 0) or 0
+    fp8 = getattr(case, "k_scale", None) is not None
+    ks = case.k_scale.to("cpu").numpy() if fp8 else None
+    vs = case.v_scale.to("cpu").numpy() if fp8 else None
+    out = np.zeros((B, h, d))
+    lse = np.zeros((B, h))
+    raw = (lambda t: t.detach().to("cpu").numpy()) if fp8 else f64
+    for b in range(B):
+        held = min(int(sl[b]), window) if window > 0 else int(sl[b])
+        for kv in range(n_kv):
+            heads = slice(kv * g, (kv + 1) * g)
+            q = f64(case.q[b:b + 1, heads])
+            if bt is None:
+                n_slots = max(held, window) if window > 0 else held
+                K = raw(case.k[b:b + 1, kv:kv + 1, :max(n_slots, 1)])
+                V = raw(case.v[b:b + 1, kv:kv + 1, :max(n_slots, 1)])
+                bt_b = None
+            else:
+                npg = max((max(held, window) if window > 0 else held) + 63, 64) // 64
+                pages = torch.as_tensor(bt[b, :npg], dtype=torch.long, device=case.k.device)
+                K = raw(case.k[pages, kv:kv + 1])
+                V = raw(case.v[pages, kv:kv + 1])
+                bt_b = np.arange(npg)[None]
+            if fp8:
+                o, l = oracle.gqa_decode_fp8(q, K, V, ks[kv:kv + 1], vs[kv:kv + 1], [int(sl[b])],
+                                             case.scale, bt_b, window)
+            else:
+                o, l = oracle.gqa_decode(q, K, V, [int(sl[b])], case.scale, bt_b, window)
+            out[b, heads], lse[b, heads] = o[0], l[0]
+    return out, lse
+
+
+def mla_full_oracle(case):
+    """Oracle latent output and lse of a whole MlaCase, one oracle call per
+    sequence on that sequence's pages (gathered in logical order)."""
+    sl = case.seqlens.to("cpu").numpy()
+    bt = case.block_table.to("cpu").numpy()
+    out = np.zeros((case.B, case.n_h, 512))
+    lse = np.zeros((case.B, case.n_h))
+    for b in range(case.B):
+        L = int(sl[b])
+        npg = max((L + 63) // 64, 1)
+        pages = torch.as_tensor(bt[b, :npg], dtype=torch.long, device=case.cache.device)
+        o, l = oracle.mla_decode_absorbed(f64(case.q_abs[b:b + 1]), f64(case.q_rope[b:b + 1]),
+                                          f64(case.cache[pages]), np.arange(npg)[None], [L],
+                                          case.scale)
+        out[b], lse[b] = o[0], l[0]
+    return out, lse
+
+
 def sample_rows(B, H, n, seed=0):
     rng = np.random.default_rng(seed)
     rows = {(0, 0), (B - 1, H - 1)}

@@ -144,9 +144,10 @@ def test_prefill_argument_checks(lib):
 
 def test_mla_batch_limit(lib):
     """The MLA decode keeps a tile table of batch + 1 ints in shared memory
-    beside five 36 KB cache stages; the largest batch that fits in the
-    227 KB a CTA may use is the limit, and one more sequence is rejected on
-    the host (INVALID_ARG) before any device query."""
+    beside five 36 KB cache stages, the 16 KB exchange and P buffers, the
+    8 KB rope part of Q and a 4 KB hand-off; the largest batch that fits in
+    the 227 KB a CTA may use is the limit (411), and one more sequence is
+    rejected on the host (INVALID_ARG) before any device query."""
     limit = lib.kvdec_mla_max_batch()
     assert limit == 411
     m = kvdec.MlaParams()

@@ -7,7 +7,7 @@ import torch
 
 import kvgen
 import oracle
-from parity import assert_attn_close, assert_lse_close, f64, sample_rows
+from parity import assert_attn_close, assert_lse_close, f64, gqa_full_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -77,24 +77,17 @@ def test_fp8_scale_is_per_kv_head(cuda_lib):
     assert not torch.allclose(out[:, :4], out2[:, :4], atol=1e-3)
 
 
-def test_fp8_full_size_llama3_8b_shape(cuda_lib):
-    """B = 32, h = 32, n_kv = 8, d = 128, seqlens U[1024, 4096] with an E4M3
-    cache, in the launch configuration the benchmark times; sampled rows
-    against the oracle."""
-    case = kvgen.gqa_case(32, 32, 8, 128, lo=1024, hi=4096, cap=4096, seed=1001,
-                          device="cuda", kv_dtype="fp8")
+@pytest.mark.parametrize("name", ["C1", "C4-GQA"])
+def test_fp8_full_size_full_output(cuda_lib, name):
+    """The Llama-3-8B-shaped and the long-context Llama-3-70B-shaped
+    workloads with an E4M3 cache, in the launch configuration the benchmark
+    times: every (b, h) row against the oracle's decode of the dequantised
+    cache."""
+    case = kvgen.config_case(name, device="cuda", kv_dtype="fp8")
     out, lse = run(cuda_lib, case)
-    rows = sample_rows(case.B, case.h, 48, seed=11)
-    sl = np_(case.seqlens)
-    ks, vs = np_(case.k_scale), np_(case.v_scale)
-    for b, hh in rows:
-        kv = hh // 4
-        L = int(sl[b])
-        K = oracle.e4m3_bits_to_f64(np_(case.k[b, kv, :L])) * ks[kv]
-        V = oracle.e4m3_bits_to_f64(np_(case.v[b, kv, :L])) * vs[kv]
-        o, l = oracle.attend(f64(case.q[b, hh:hh + 1]), K, V, case.scale)
-        assert_attn_close(out[b, hh:hh + 1], o, f"row {b},{hh}")
-        assert_lse_close(lse[b, hh:hh + 1], l, f"lse {b},{hh}")
+    ref, lref = gqa_full_oracle(case)
+    assert_attn_close(out, ref, name)
+    assert_lse_close(lse, lref, name)
 
 
 WIN = [

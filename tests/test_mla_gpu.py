@@ -38,7 +38,9 @@ def test_many_short_sequences(cuda_lib):
     tile scan carries a sequence, and the tile table fills its shared
     memory."""
     g = torch.Generator().manual_seed(5)
-    sl = torch.randint(0, 200, (cuda_lib.load().kvdec_mla_max_batch(),), generator=g).tolist()
+    sl = torch.randint(0, 200, (cuda_lib.load().kvdec_mla_max_batch(),), generator=g)
+    sl[::37] = 0                         # some sequences are empty
+    sl = sl.tolist()
     case = kvgen.mla_case(len(sl), 128, seqlens=sl, seed=217, device="cuda")
     out, lse = run(cuda_lib, case)
     ref, lref = mla_full_oracle(case)

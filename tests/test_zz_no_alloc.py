@@ -3,9 +3,9 @@ device memory (a plugin inside a runtime that owns all device memory, a
 serving loop that allows no allocation while decoding).  It keeps its split
 scratch in a fixed array inside the library, so these tests check, through
 the C ABI, that it gives the same results as kvdec_gqa_decode with a caller
-workspace -- on two calls in a row, the second finding whatever the first
-left in the shared array -- and that problems too big for the array are
-rejected with a clear error.
+workspace and as the fp64 oracle -- on two calls in a row, the second
+finding whatever the first left in the shared array -- and that problems too
+big for the array are rejected with a clear error.
 
 This file is collected last on purpose: if it fails, a run stopped at the
 first failure has already run every other test."""
@@ -16,7 +16,7 @@ import torch
 
 import kvgen
 from decode_attention_kv_softmax_b300 import kvdec
-from parity import assert_attn_close, assert_lse_close, f64
+from parity import assert_attn_close, assert_lse_close, f64, gqa_full_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +37,11 @@ def test_matches_workspace_entry_point_on_two_calls(cuda_lib):
         torch.cuda.synchronize()
         assert_attn_close(out, f64(ref), f"call {i}")
         assert_lse_close(lse, f64(lref), f"call {i}")
+        # and against the oracle, so that a defect shared by both entry
+        # points cannot pass
+        oref, olse = gqa_full_oracle(case)
+        assert_attn_close(out, oref, f"call {i} vs oracle")
+        assert_lse_close(lse, olse, f"call {i} vs oracle")
 
 
 def test_rejects_problems_beyond_the_array(cuda_lib):

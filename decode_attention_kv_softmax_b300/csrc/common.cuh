@@ -245,6 +245,14 @@ KVDEC_DEVINL void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared memory through L2 only (data
+// other SMs wrote), completed by cp_async_wait_all.
+KVDEC_DEVINL void cp_async16(uint32_t dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+KVDEC_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+KVDEC_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 // Bring a tensor-map box into L2 ahead of its load (no shared memory, no
 // barrier; boxes past the tensor's edge are ignored).
 KVDEC_DEVINL void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {

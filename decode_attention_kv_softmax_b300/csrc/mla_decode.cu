@@ -494,10 +494,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(hbar);
             }
-            // ---- probabilities (base 2) -> P(j) in shared memory, K-major with the
-            // 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r & 7)),
-            // once PV(j-1) has read the buffer (at a sequence's first page: once
-            // the previous sequence's flush, which stages through it, is done)
+            // ---- probabilities (base 2) -> registers, packed to bf16 pairs; they
+            // are computed before the wait for the P buffer, so only the
+            // stores below wait for PV(j-1)
+            uint32_t pk[32];
+            float lsum;
+            {
+                float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = fast_exp2(fmaf(s[2 * i], sl2, -m_new));
+                    const float p1 = fast_exp2(fmaf(s[2 * i + 1], sl2, -m_new));
+                    ls[i & 3] += p0 + p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            }
+            l_g = l_g * fast_exp2(m_g - m_new) + lsum;
+            m_g = m_new;
+            if (pre_last) {
+                *hout = make_float2(m_new, l_g);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(hbar);
+            }
+            // ---- P(j) -> shared memory, K-major with the 128-byte swizzle
+            // (16-byte chunk c of row r at chunk c ^ (r & 7)), once PV(j-1) has
+            // read the buffer (at a sequence's first page: once the previous
+            // sequence's flush, which stages through it, is done)
             if (PB == 2) {
                 if (j >= 2 && !wait_or_abort(bar(B_PV_DONE + g), (uint32_t)(((j - 2) >> 1) & 1), abort_word, a.err,
                                              a.timeout_ns))
@@ -510,27 +533,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                 break;
             }
             uint8_t* prow = smem + L::kOffP + (PB == 2 ? g * kPBytes : 0) + row * 128;
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float p0 = fast_exp2(fmaf(s[8 * c + 2 * i], sl2, -m_new));
-                    const float p1 = fast_exp2(fmaf(s[8 * c + 2 * i + 1], sl2, -m_new));
-                    ls[i] += p0 + p1;
-                    pk[i] = pack_bf16x2(p0, p1);
-                }
-                *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            const float lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-            l_g = l_g * fast_exp2(m_g - m_new) + lsum;
-            m_g = m_new;
-            if (pre_last) {
-                *hout = make_float2(m_new, l_g);
-                __syncwarp();
-                if (lane == 0) mbar_arrive(hbar);
-            }
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(prow + ((c ^ (row & 7)) << 4)) =
+                    make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
             // ---- rescale O where the running max moved (rare): after PV(j-1), before PV(j)
             if (__any_sync(0xffffffffu, resc)) {
                 if (!wait_or_abort(bar(B_PV_DONE + (g ^ 1)), (uint32_t)(((j - 1) >> 1) & 1), abort_word, a.err,
@@ -646,9 +652,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
                                    ? 1
                                    : 0;
                     last = __shfl_sync(0xffffffffu, last, 0);
-                    // the last piece to arrive: the merge runs after the pages (at most
-                    // two per quadrant: only an item's first and last sequences are cut)
+                    // the last piece to arrive: every piece has counted, so the
+                    // counter goes back to 0 at once (a replayed launch keeps its
+                    // epoch and must start from zero); the merge runs after the
+                    // pages (at most two per quadrant: only an item's first and
+                    // last sequences are cut)
                     if (last && lane == 0) {
+                        a.counters[((size_t)cur.b * 2 + rank) * 4 + qd] = 0ull;
                         const int e = atomicAdd(pend + 4 * qd, 1);
                         if (e < 2) pend[4 * qd + 1 + e] = cur.b;
                     }

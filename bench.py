@@ -60,6 +60,7 @@ WORKLOADS = {
     "C4-MLA": "long ragged MLA absorbed decode B=8 n_h=128 seqlens U[16384,131072] paged",
     "C4-GQA": "long ragged Llama-3-70B-shaped GQA decode B=8 h=64 n_kv=8 d=128 seqlens U[16384,131072] paged",
     "P-MLA": "DeepSeek-V3-shaped MLA prefill chunk, non-absorbed: 4096 tokens, 128 heads, causal (expand + attention)",
+    "combine": "stand-alone LSE combine of split partials: 16 pieces of [32768 rows, 128] fp32 (268 MB)",
 }
 # the parts (single-family workloads) one step of each workload runs
 PARTS = {"C4": ["C4-GQA", "C4-MLA"]}
@@ -657,8 +658,69 @@ class Part:
                 f"L2-resident in part (the workload is smaller than L2)")
 
 
+def bench_combine(args):
+    """--config combine: one step = kvdec_combine_splits over 16 normalised
+    partials of 32768 rows x 128 (the merge of [ARG] §五.2 on its own);
+    value in GB/s of algorithmic bytes (every partial and lse read once, out
+    and lse written once)."""
+    import torch
+    from decode_attention_kv_softmax_b300 import kvdec
+    kvdec.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream()
+    hbm_peak, _, _, peak_src = measured_peaks()
+    S, R, D = 16, 32768, 128
+    g = torch.Generator(device=dev).manual_seed(1009)
+    sets = [(torch.randn((S, R, D), generator=g, device=dev), torch.randn((S, R), generator=g, device=dev))
+            for _ in range(2)]
+    outs = [torch.empty((R, D), device=dev) for _ in range(2)]
+    alg = S * R * (D + 1) * 4 + R * (D + 1) * 4
+
+    def step(i):
+        po, pl = sets[i & 1]
+        kvdec.combine_splits(po, pl, out=outs[i & 1], stream=stream)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    clk = ClockSampler(0)
+    clk.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        evs[i][0].record(stream)
+        step(i)
+        evs[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    ms = t0.elapsed_time(t1) / args.steps
+    per = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]
+    avg = sum(per) / len(per)
+    ach = alg / (avg * 1e-6) / 1e9
+    line = {"metric": METRIC, "value": alg / (ms * 1e-3) / 1e9, "unit": "GB/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOADS["combine"], "name": "combine",
+                       "l2": "two 277 MB input sets alternated (> 2x L2)"},
+            "roofline": {"bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": ach / hbm_peak,
+                         "traffic": ncu_traffic("combine_kernel@combine", ["combine.cu", "common.cuh"]),
+                         "kernel": "combine_kernel", "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
+                         "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg,
+                         "median_launch_us": statistics.median(per)},
+            "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": args.steps}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
+    if args.config == "combine":
+        if args.impl == "reference" or args.gpus != 1 or int(os.environ.get("RANK", "0")) != 0:
+            return
+        bench_combine(args)
+        return
     if args.config == "P-MLA":
         if args.gpus != 1 or int(os.environ.get("RANK", "0")) != 0:
             return
@@ -699,7 +761,15 @@ def main():
 
     clk = ClockSampler(local)
     clk.start()
-    time.sleep(0.3)
+    # keep the GPU busy while the sampler starts (an idle GPU lowers its
+    # clocks, and a short timed region would start below them)
+    t_busy, i = time.time(), 0
+    while time.time() - t_busy < 0.3:
+        step(i)
+        i += 1
+        if i % 4 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in parts]
            for _ in range(args.steps)]
     host_us = []
@@ -723,6 +793,19 @@ def main():
             step(i)
         torch.cuda.synchronize()
     clocks = clk.stop()
+
+    # host cost of enqueueing one step, on short bursts that cannot fill the
+    # launch queue (inside the timed region the enqueue loop also waits for
+    # queue space whenever the GPU is the slower side)
+    burst_us = []
+    for r in range(10):
+        torch.cuda.synchronize()
+        step(0)                       # the first call after a synchronize is not timed
+        h0 = time.perf_counter()
+        for i in range(16):
+            step(i)
+        burst_us.append((time.perf_counter() - h0) / 16 * 1e6)
+    torch.cuda.synchronize()
 
     # back-to-back cross-check: M decode launches of a part between one event pair
     b2b = {}
@@ -850,8 +933,10 @@ def main():
             "data": "synthetic", "config": cfg,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
             "gpu_launches": 2 * len(parts) * args.steps,
-            "host_enqueue_us_per_step": {"median": statistics.median(host_us),
-                                         "mean": sum(host_us) / len(host_us)}}
+            "host_enqueue_us_per_step": {"median": statistics.median(burst_us),
+                                         "note": "host time to enqueue one step (all parts' append "
+                                                 "and decode calls), bursts of 16 steps",
+                                         "timed_region_median": statistics.median(host_us)}}
     print(json.dumps(line), flush=True)
     if ws > 1:
         import torch.distributed as dist

@@ -495,6 +495,7 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
     a.scale_log2 = (float)(scale * 1.4426950408889634);
     a.min_tiles = 4;
+    a.seg_cost = kvdec::kMlaSeqStartCost;
     a.timeout_ns = kvdec::kDefaultTimeoutNs;
     cudaError_t e = kvdec::launch_mla(maps, a, pl.pairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");

@@ -252,6 +252,11 @@ KVDEC_DEVINL void cp_async16(uint32_t dst_smem, const void* src) {
 }
 KVDEC_DEVINL void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 KVDEC_DEVINL void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// wait until at most N of this thread's cp.async groups are pending
+template <int N>
+KVDEC_DEVINL void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
 
 // Bring a tensor-map box into L2 ahead of its load (no shared memory, no
 // barrier; boxes past the tensor's edge are ignored).

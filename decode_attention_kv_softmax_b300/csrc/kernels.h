@@ -88,8 +88,13 @@ struct MlaArgs {
     int out_bf16;
     float scale_log2;
     int min_tiles;
+    int seg_cost;                   // start cost of a sequence, in pages (schedule.cuh)
     uint64_t timeout_ns;
 };
+
+// Start cost of a sequence in the MLA decode schedule, in pages: loading a
+// new Q into TMEM and flushing O takes about as long as this many pages.
+constexpr int kMlaSeqStartCost = 4;
 
 struct MlaProjArgs {
     const __nv_bfloat16* x;   // absorb: q_nope [B, H, 128]; project: latent [B, H, 512]

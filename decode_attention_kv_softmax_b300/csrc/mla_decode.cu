@@ -145,6 +145,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     S.upb = 1;
     S.T = cum[a.B];
     S.W = effective_items(S.T, npairs, a.min_tiles);
+    S.c = a.seg_cost;
     const int w = pair;
     const long long t_begin = (w < S.W && S.T > 0) ? S.item_begin(w) : 0;
     const long long t_end = (w < S.W && S.T > 0) ? S.item_begin(w + 1) : 0;
@@ -675,64 +676,108 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
         }
 
         // ---- merges of the sequences whose last piece this CTA wrote, by
-        // log-sum-exp ([ARG] §五.2).  Both groups' warps of a quadrant take 128
-        // of the CTA's 256 columns each, 16 rows of loads in flight per warp
-        // (the registers of the page loop are free by now).
+        // log-sum-exp ([ARG] §五.2).  Warp (g, qd) merges rows [32 qd, 32 qd + 32)
+        // x columns [256 rank + 128 g, +128) of every piece.  The cache stages
+        // are free by now: each warp streams 8-row blocks of the pieces (4 KB,
+        // then the 8 rows' lse) through its own ring of kMD slots there with
+        // cp.async, so that several pieces are in flight at once.
         named_barrier(1, 32 * kSoftWarps);
         __threadfence();
         {
+            constexpr int kMD = 5;                   // ring slots per warp
+            constexpr int kSlotBytes = 4096 + 32;    // [8 rows][128 fp32], lse[8]
+            static_assert(kSoftWarps * kMD * kSlotBytes <= NS * kStageBytes, "the merge rings fit in the stages");
+            const uint32_t wring = sKV + (uint32_t)(warp * kMD * kSlotBytes);
+            const uint8_t* wring_p = smem + L::kOffKV + warp * kMD * kSlotBytes;
             const float* plse = a.part_lse + (size_t)rank * (2 * npairs) * kHeads;
             const int nm = min(pend[4 * qd], 2);
             const int c0 = 256 * (int)rank + 128 * g;
+            fence_proxy_async();   // the stages were last written by TMA and read by the MMAs
             for (int e = 0; e < nm; ++e) {
                 const int b = pend[4 * qd + 1 + e];
                 const int npc = S.num_pieces(b, 0);
                 int w0, kind0;
                 S.first_piece(b, 0, w0, kind0);
+                auto slot_of = [&](int s2) { return 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0); };
+                const int nk = 4 * npc;   // blocks: row block rb (outer) x piece s2
+                // block k -> ring slot k % kMD; past the last block an empty
+                // group keeps the count of pending groups uniform
+                auto issue = [&](int k) {
+                    if (k < nk) {
+                        const int rb = k / npc, s2 = k - rb * npc;
+                        const int sl = slot_of(s2);
+                        const uint32_t dst = wring + (uint32_t)((k % kMD) * kSlotBytes);
+                        const float* src = a.part_o + ((size_t)sl * kHeads + qd * 32 + rb * 8) * 512 + c0 + 4 * lane;
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) cp_async16(dst + (uint32_t)(r * 512 + lane * 16), src + (size_t)r * 512);
+                        if (lane < 2)
+                            cp_async16(dst + 4096u + (uint32_t)(lane * 16),
+                                       plse + (size_t)sl * kHeads + qd * 32 + rb * 8 + 4 * lane);
+                    }
+                    cp_async_commit();
+                };
+#pragma unroll
+                for (int k = 0; k < kMD - 1; ++k) issue(k);
+                // max and denominator of row 32 qd + lane over the pieces, four
+                // lse loads in flight
                 float M = -INFINITY, den = 0.f;
-                for (int s2 = 0; s2 < npc; ++s2) {
-                    const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                    M = fmaxf(M, __ldcg(plse + (size_t)sl * kHeads + row));
-                }
-                for (int s2 = 0; s2 < npc; ++s2) {
-                    const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                    const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
-                    den += (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e);
+                for (int s2 = 0; s2 < npc; s2 += 4) {
+                    float ls[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        ls[u] = s2 + u < npc ? __ldcg(plse + (size_t)slot_of(s2 + u) * kHeads + row) : -INFINITY;
+                    const float Mn = fmaxf(fmaxf(M, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
+                    if (Mn != -INFINITY) {
+                        den = (M == -INFINITY) ? 0.f : den * fast_exp2((M - Mn) * kLog2e);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) den += (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - Mn) * kLog2e);
+                        M = Mn;
+                    }
                 }
                 if (rank == 0 && g == 0 && a.lse) a.lse[(size_t)b * kHeads + row] = den > 0.f ? M + __logf(den) : -INFINITY;
                 const float invd = den > 0.f ? 1.f / den : 0.f;
-                for (int r0 = 0; r0 < 32; r0 += 16) {
-                    float4 acc[16];
+                float4 acc[8];
+                float mr[8], ir[8];
+                for (int k = 0; k < nk; ++k) {
+                    const int rb = k / npc, s2 = k - rb * npc;
+                    if (s2 == 0) {
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    for (int s2 = 0; s2 < npc; ++s2) {
-                        const int sl = 2 * (w0 + s2) + (s2 == 0 ? kind0 : 0);
-                        const float ls = __ldcg(plse + (size_t)sl * kHeads + row);
-                        const float wm = (ls == -INFINITY) ? 0.f : fast_exp2((ls - M) * kLog2e) * invd;
-                        const float4* src = reinterpret_cast<const float4*>(
-                            a.part_o + ((size_t)sl * kHeads + qd * 32 + r0) * 512 + c0) + lane;
-                        float4 x[16];
-#pragma unroll
-                        for (int v = 0; v < 16; ++v) x[v] = __ldcg(src + (size_t)v * 128);
-#pragma unroll
-                        for (int v = 0; v < 16; ++v) {
-                            const float wgt = __shfl_sync(0xffffffffu, wm, r0 + v);
-                            acc[v].x = fmaf(wgt, x[v].x, acc[v].x);
-                            acc[v].y = fmaf(wgt, x[v].y, acc[v].y);
-                            acc[v].z = fmaf(wgt, x[v].z, acc[v].z);
-                            acc[v].w = fmaf(wgt, x[v].w, acc[v].w);
+                        for (int r = 0; r < 8; ++r) {
+                            acc[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            mr[r] = __shfl_sync(0xffffffffu, M, rb * 8 + r);
+                            ir[r] = __shfl_sync(0xffffffffu, invd, rb * 8 + r);
                         }
                     }
+                    issue(k + kMD - 1);
+                    cp_async_wait_group<kMD - 1>();   // this lane's copies of block k have landed
+                    __syncwarp();                     // ... and every lane's
+                    const uint8_t* blk = wring_p + (k % kMD) * kSlotBytes;
+                    const float* bl = reinterpret_cast<const float*>(blk + 4096);
 #pragma unroll
-                    for (int v = 0; v < 16; ++v) {
-                        const size_t off = ((size_t)b * kHeads + qd * 32 + r0 + v) * 512 + c0 + 4 * lane;
-                        if (a.out_bf16)
-                            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
-                                make_uint2(pack_bf16x2(acc[v].x, acc[v].y), pack_bf16x2(acc[v].z, acc[v].w));
-                        else
-                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[v];
+                    for (int r = 0; r < 8; ++r) {
+                        const float ls = bl[r];
+                        const float wm = (ls == -INFINITY) ? 0.f : fast_exp2((ls - mr[r]) * kLog2e) * ir[r];
+                        const float4 x = *reinterpret_cast<const float4*>(blk + r * 512 + lane * 16);
+                        acc[r].x = fmaf(wm, x.x, acc[r].x);
+                        acc[r].y = fmaf(wm, x.y, acc[r].y);
+                        acc[r].z = fmaf(wm, x.z, acc[r].z);
+                        acc[r].w = fmaf(wm, x.w, acc[r].w);
+                    }
+                    __syncwarp();   // every lane has read the slot before it is refilled
+                    if (s2 == npc - 1) {
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const size_t off = ((size_t)b * kHeads + qd * 32 + rb * 8 + r) * 512 + c0 + 4 * lane;
+                            if (a.out_bf16)
+                                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) =
+                                    make_uint2(pack_bf16x2(acc[r].x, acc[r].y), pack_bf16x2(acc[r].z, acc[r].w));
+                            else
+                                *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc[r];
+                        }
                     }
                 }
+                cp_async_wait_all();
+                __syncwarp();
             }
         }
     }

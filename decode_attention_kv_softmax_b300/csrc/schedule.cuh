@@ -15,6 +15,19 @@
 // Partial slots: item w owns slots 2w (the piece holding the item's first
 // tile) and 2w+1 (the piece holding its last tile, when that is a different
 // unit).  Only these two pieces of an item can be incomplete units.
+//
+// Unit start cost.  Starting a unit costs a CTA more than a tile where the
+// switch is slow (the MLA kernel loads a new Q into TMEM and flushes O at
+// every switch), so the cut points can be chosen on a cost axis instead of
+// the tile axis: unit u = b * upb + j (empty units included) occupies
+// [u c + first tile of u, ...), i.e. c cost units of start overhead and then
+// one per tile, and the cost position of tile t of unit u is t + c (u + 1).
+// With total cost C = T + c B upb, item w covers the cost range
+// [floor(C w / W), floor(C (w+1) / W)) and starts at the first tile whose
+// cost position lies in it.  Cost positions grow strictly with t, so the
+// items still cover consecutive tile ranges (an item can be empty when a cut
+// lands in overhead) and a unit's pieces still sit in consecutive items;
+// c = 0 is the plain tile split above.
 #pragma once
 
 #include "common.cuh"
@@ -29,15 +42,51 @@ struct TileSchedule {
     int upb;
     long long T;  // total tiles
     int W;        // work items (>= 1)
+    int c = 0;    // start cost of a unit, in tiles
 
     KVDEC_HDINL int ntiles(int b) const { return cum[b + 1] - cum[b]; }
-    KVDEC_HDINL long long item_begin(int w) const { return T * (long long)w / W; }
-    // the item holding global tile t
-    KVDEC_HDINL int item_of(long long t) const {
-        return (int)(((t + 1) * (long long)W - 1) / T);
+    KVDEC_HDINL long long total_cost() const { return T + (long long)c * B * upb; }
+    // cost position of tile t, which is tile lt of unit (b, j)
+    KVDEC_HDINL long long cost_of(int b, int j, long long t) const {
+        return t + (long long)c * ((long long)b * upb + j + 1);
+    }
+    // first tile of item w (T for w = W)
+    KVDEC_HDINL long long item_begin(int w) const {
+        if (c == 0) return T * (long long)w / W;
+        const long long C = total_cost();
+        const long long X = C * (long long)w / W;   // the item's first cost position
+        if (X >= C) return T;
+        // the last sequence whose first unit starts (overhead included) at or before X
+        int lo = 0, hi = B;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if ((long long)cum[mid] * upb + (long long)c * mid * upb <= X) lo = mid;
+            else hi = mid;
+        }
+        const int b = lo, nt = ntiles(b);
+        const long long s0 = (long long)cum[b] * upb + (long long)c * b * upb;
+        long long j = (X - s0) / (nt + c);
+        if (j > upb - 1) j = upb - 1;
+        const long long off = X - s0 - j * (nt + c);   // into unit (b, j): c of overhead, then its tiles
+        const long long first = (long long)cum[b] * upb + j * nt;
+        if (off <= c) return first;
+        const long long lt = off - c;
+        return first + (lt < nt ? lt : nt);   // past the unit's tiles: the next unit's first tile
+    }
+    // the item holding tile t of unit (b, j)
+    KVDEC_HDINL int item_of_in(int b, int j, long long t) const {
+        const long long x = cost_of(b, j, t);
+        return (int)(((x + 1) * (long long)W - 1) / total_cost());
     }
     KVDEC_HDINL long long unit_begin(int b, int j) const {
         return (long long)cum[b] * upb + (long long)j * ntiles(b);
+    }
+    // the item holding global tile t
+    KVDEC_HDINL int item_of(long long t) const {
+        if (c == 0) return (int)(((t + 1) * (long long)W - 1) / T);
+        int b, j, lt;
+        locate(t, b, j, lt);
+        return item_of_in(b, j, t);
     }
     // (b, j, lt) of global tile t, 0 <= t < T
     KVDEC_HDINL void locate(long long t, int& b, int& j, int& lt) const {
@@ -56,18 +105,18 @@ struct TileSchedule {
     // number of pieces unit (b, j) is cut into, and the slot of piece s
     KVDEC_HDINL int num_pieces(int b, int j) const {
         const long long t0 = unit_begin(b, j);
-        return item_of(t0 + ntiles(b) - 1) - item_of(t0) + 1;
+        return item_of_in(b, j, t0 + ntiles(b) - 1) - item_of_in(b, j, t0) + 1;
     }
     // first item holding unit (b, j) and the slot kind of its first piece;
     // piece s >= 1 lives in slot 2 * (w0 + s)
     KVDEC_HDINL void first_piece(int b, int j, int& w0, int& kind0) const {
         const long long t0 = unit_begin(b, j);
-        w0 = item_of(t0);
+        w0 = item_of_in(b, j, t0);
         kind0 = (t0 != item_begin(w0)) ? 1 : 0;
     }
     KVDEC_HDINL int piece_slot(int b, int j, int s) const {
         const long long t0 = unit_begin(b, j);
-        const int w0 = item_of(t0);
+        const int w0 = item_of_in(b, j, t0);
         const int kind = (s == 0 && t0 != item_begin(w0)) ? 1 : 0;
         return 2 * (w0 + s) + kind;
     }

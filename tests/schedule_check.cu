@@ -6,7 +6,9 @@
 //   * partial slots are unique across the grid and lie in [0, 2W);
 //   * the pieces recorded for each unit match num_pieces / piece_slot, the
 //     functions the merging CTA uses to find them;
-//   * a unit is written directly exactly when it lies inside one item.
+//   * a unit is written directly exactly when it lies inside one item;
+//   * with a unit start cost c > 0, item_begin is the first tile whose cost
+//     position reaches the item's cut, found by brute force.
 #include <cstdio>
 #include <cstdlib>
 #include <map>
@@ -31,7 +33,7 @@ static int fails = 0;
         }                                      \
     } while (0)
 
-static void run_case(const std::vector<int>& lens, int upb, int grid, int min_tiles) {
+static void run_case(const std::vector<int>& lens, int upb, int grid, int min_tiles, int c = 0) {
     const int B = (int)lens.size();
     std::vector<int> cum(B + 1, 0);
     for (int b = 0; b < B; ++b) cum[b + 1] = cum[b] + (lens[b] + 63) / 64;
@@ -41,7 +43,27 @@ static void run_case(const std::vector<int>& lens, int upb, int grid, int min_ti
     S.upb = upb;
     S.T = (long long)cum[B] * upb;
     S.W = effective_items(S.T, grid, min_tiles);
+    S.c = c;
     CHECK(S.W >= 1 && S.W <= grid, "W=%d grid=%d", S.W, grid);
+    // item boundaries against a brute-force walk of the cost axis
+    if (S.T > 0) {
+        std::vector<long long> cost;   // cost position of every tile, in order
+        for (int b = 0; b < B; ++b)
+            for (int j = 0; j < upb; ++j)
+                for (int lt = 0; lt < S.ntiles(b); ++lt)
+                    cost.push_back((long long)cost.size() + (long long)c * ((long long)b * upb + j + 1));
+        const long long C = S.T + (long long)c * B * upb;
+        for (int w = 0; w <= S.W; ++w) {
+            const long long cut = C * w / S.W;
+            long long want = S.T;
+            for (long long t = 0; t < S.T; ++t)
+                if (cost[t] >= cut) {
+                    want = t;
+                    break;
+                }
+            CHECK(S.item_begin(w) == want, "c=%d item_begin(%d)=%lld want %lld", c, w, S.item_begin(w), want);
+        }
+    }
     // expected global order
     std::vector<std::tuple<int, int, int>> order;
     for (int b = 0; b < B; ++b)
@@ -119,7 +141,9 @@ int main() {
     run_case({64, 65, 128, 129}, 3, 5, 1);
     run_case({4096}, 8, 296, 8);
     run_case({0}, 4, 3, 8);
-    cases += 5;
+    run_case({64, 0, 0, 4096, 1}, 1, 74, 4, 5);
+    run_case({3000, 100, 0, 70000}, 2, 37, 1, 8);
+    cases += 7;
     for (int it = 0; it < 3000; ++it) {
         const int B = 1 + rng() % 40;
         std::vector<int> lens(B);
@@ -128,7 +152,8 @@ int main() {
         const int upb = 1 + rng() % 9;
         const int grid = 1 + rng() % 400;
         const int min_tiles = 1 + rng() % 10;
-        run_case(lens, upb, grid, min_tiles);
+        const int c = (it % 2 == 0) ? 0 : (int)(rng() % 9);
+        run_case(lens, upb, grid, min_tiles, c);
         ++cases;
     }
     if (fails) {

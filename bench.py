@@ -687,6 +687,11 @@ def bench_combine(args):
     time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # a single ~55 us kernel per step is shorter than the host's enqueue of
+    # a step: hold the stream with a spin kernel (before the timed region)
+    # while all steps are enqueued, so the launches run back to back and the
+    # per-launch events time the kernel, not host gaps
+    torch.cuda._sleep(int(args.steps * 4e5))
     t0.record(stream)
     for i in range(args.steps):
         evs[i][0].record(stream)
@@ -709,7 +714,8 @@ def bench_combine(args):
                          "traffic": ncu_traffic("combine_kernel@combine", ["combine.cu", "common.cuh"]),
                          "kernel": "combine_kernel", "peak_source": f"{peak_src} hbm_gbs (copy, burst)",
                          "algorithmic_bytes_per_launch": alg, "avg_launch_us": avg,
-                         "median_launch_us": statistics.median(per)},
+                         "median_launch_us": statistics.median(per),
+                         "timing": "launches queued behind a spin kernel, run back to back"},
             "cpu_baseline": None, "e2e": None, "clocks": clocks, "gpu_launches": args.steps}
     print(json.dumps(line), flush=True)
 

@@ -252,9 +252,17 @@ def max_over_ranks(x, ws):
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.item()
+
+
+def replica_throughput(units_per_rank, seconds_per_rank, ws):
+    """Whole-job throughput of ws independent replicas: the units all ranks
+    processed over the slowest rank's time (every rank processes the same
+    units per step)."""
+    return ws * units_per_rank / max_over_ranks(seconds_per_rank, ws)
 
 
 def l2_bytes(dev):
@@ -825,10 +833,10 @@ def main():
         torch.cuda.synchronize()
         b2b[part.name] = e0.elapsed_time(e1) / M * 1e3
 
+    step_bytes = sum(p.step_bytes(i) for p in parts for i in range(args.steps)) / args.steps
+    value = replica_throughput(step_bytes * args.steps, total_ms * 1e-3, ws) / 1e9
     total_ms = max_over_ranks(total_ms, ws)
     ms_per_step = total_ms / args.steps
-    step_bytes = sum(p.step_bytes(i) for p in parts for i in range(args.steps)) / args.steps
-    value = ws * step_bytes / (ms_per_step * 1e-3) / 1e9
 
     kernels = {}
     for k, part in enumerate(parts):
@@ -937,10 +945,12 @@ def main():
         stream.wait_event(lg["out_read"])
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / max(n_e2e, 1), ws)
     e2e_bytes = sum(p.step_bytes(0) for p in parts)
+    e2e_rank_ms = e0.elapsed_time(e1) / max(n_e2e, 1)
+    e2e_value = replica_throughput(e2e_bytes, e2e_rank_ms * 1e-3, ws) / 1e9
+    e2e_ms = max_over_ranks(e2e_rank_ms, ws)
     e2e = None if not n_e2e else {
-        "value": ws * e2e_bytes / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "value": e2e_value, "unit": "GB/s",
         "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
         "steps": n_e2e, "note": "per-step inputs (queries, the new token's cache entries, positions, "
                                 "seqlens) copied from pinned host memory, outputs and lse read back, "

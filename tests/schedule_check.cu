@@ -143,7 +143,15 @@ int main() {
     run_case({0}, 4, 3, 8);
     run_case({64, 0, 0, 4096, 1}, 1, 74, 4, 5);
     run_case({3000, 100, 0, 70000}, 2, 37, 1, 8);
-    cases += 7;
+    {
+        // hundreds of empty sequences and one long one: items without tiles
+        std::vector<int> sparse(300, 0);
+        sparse[250] = 5000;
+        sparse[17] = 5;
+        run_case(sparse, 1, 74, 4, 4);
+        run_case(sparse, 1, 4, 4, 4);
+    }
+    cases += 9;
     for (int it = 0; it < 3000; ++it) {
         const int B = 1 + rng() % 40;
         std::vector<int> lens(B);

@@ -50,6 +50,26 @@ def test_many_short_sequences(cuda_lib):
     assert empty and all(torch.all(out[b] == 0) for b in empty)
 
 
+@pytest.mark.parametrize("max_ctas", [8, 0])
+def test_work_items_without_pages(cuda_lib, max_ctas):
+    """The split schedule charges every sequence start (empty ones too) a
+    few pages, so with hundreds of empty sequences and one long one the cut
+    points can fall where no page lies: some CTA pairs get no pages, the
+    long sequence's pieces sit in consecutive work items, and the empty
+    sequences are still written (0 and lse = -inf)."""
+    sl = [0] * 300
+    sl[250] = 5000      # with the full grid: cut into two pieces, most items empty
+    sl[17] = 5
+    case = kvgen.mla_case(len(sl), 128, seqlens=sl, seed=219, device="cuda")
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas)
+    ref, lref = mla_full_oracle(case)
+    assert_attn_close(out, ref, f"sparse max_ctas={max_ctas}")
+    assert_lse_close(lse, lref)
+    empty = [b for b, s in enumerate(sl) if s == 0]
+    assert all(torch.all(out[b] == 0) for b in empty)
+    assert torch.isneginf(lse[empty]).all()
+
+
 @pytest.mark.parametrize("max_ctas", [2, 4, 6, 14, 0])
 def test_split_invariance(cuda_lib, max_ctas):
     """Sequences cut across CTA pairs merge to the same result."""

@@ -17,10 +17,14 @@ def np_(t):
 
 
 def run(kv, case, **kw):
+    """One decode through the C ABI; a valid launch leaves the device error
+    word clear."""
+    flag = kv.new_error_flag()
     out, lse = kv.gqa_decode(case.q, case.k, case.v, case.seqlens, case.block_table,
                              scale=case.scale, k_scale=case.k_scale, v_scale=case.v_scale,
-                             window=case.window, **kw)
+                             window=case.window, error_flag=flag, **kw)
     torch.cuda.synchronize()
+    assert flag.item() == 0, f"device error word {flag.item():#x}"
     return out, lse
 
 

@@ -12,9 +12,13 @@ pytestmark = pytest.mark.gpu
 
 
 def run(kv, case, **kw):
+    """One decode through the C ABI; a valid launch leaves the device error
+    word clear (no bad index, no wait that ran out)."""
+    flag = kv.new_error_flag()
     out, lse = kv.gqa_decode(case.q, case.k, case.v, case.seqlens, case.block_table,
-                             scale=case.scale, **kw)
+                             scale=case.scale, error_flag=flag, **kw)
     torch.cuda.synchronize()
+    assert flag.item() == 0, f"device error word {flag.item():#x}"
     return out, lse
 
 
@@ -135,6 +139,20 @@ def test_mqa_equals_repeated_mha(cuda_lib):
     out2, _ = cuda_lib.gqa_decode(case.q, k_rep, v_rep, case.seqlens, scale=case.scale)
     torch.cuda.synchronize()
     assert_attn_close(out1, f64(out2), "MQA vs repeated MHA")
+
+
+@pytest.mark.parametrize("kv_dtype", ["bf16", "fp8"])
+def test_launch_returns_promptly(cuda_lib, kv_dtype):
+    """A full-size launch returns in well under the kernel's 2 s bounded-wait
+    limit with the error word clear: no wait of the kernel runs out."""
+    import time
+    case = kvgen.config_case("C1", device="cuda", kv_dtype=kv_dtype)
+    kw = {} if kv_dtype == "bf16" else dict(k_scale=case.k_scale, v_scale=case.v_scale)
+    run(cuda_lib, case, **kw)                 # warm-up (plan, tensor maps)
+    t0 = time.perf_counter()
+    for _ in range(5):
+        run(cuda_lib, case, **kw)
+    assert (time.perf_counter() - t0) / 5 < 0.2
 
 
 @pytest.mark.parametrize("name", ["C1", "C2-MHA", "C2-MQA", "C4-GQA"])

@@ -12,9 +12,13 @@ pytestmark = pytest.mark.gpu
 
 
 def run(kv, case, **kw):
+    """One decode through the C ABI; a valid launch leaves the device error
+    word clear (no bad index, no wait that ran out)."""
+    flag = kv.new_error_flag()
     out, lse = kv.mla_decode_absorbed(case.q_abs, case.q_rope, case.cache, case.block_table,
-                                      case.seqlens, scale=case.scale, **kw)
+                                      case.seqlens, scale=case.scale, error_flag=flag, **kw)
     torch.cuda.synchronize()
+    assert flag.item() == 0, f"device error word {flag.item():#x}"
     return out, lse
 
 

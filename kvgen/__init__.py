@@ -90,6 +90,9 @@ class MlaCase:
     block_table: torch.Tensor  # int32 [B, max_blocks]
     scale: float
     meta: dict = field(default_factory=dict)
+    # E4M3 cache: cache holds uint8 codes and this the fp32 scales
+    # [c_kv scale, k_R scale]
+    kv_scale: torch.Tensor | None = None
 
     @property
     def B(self):
@@ -206,8 +209,29 @@ def fp8_codes(x: torch.Tensor, g, device):
     return codes, scale
 
 
+def mla_fp8_codes(cache: torch.Tensor, g, device):
+    """Stand-in for a quantised E4M3 latent cache: the drawn N(0,1) c_kv
+    values times a spread sigma_c and the k_R values times sigma_R, both
+    ~ U[0.25, 4] (so that the two scales differ and a swap is visible),
+    cast by torch to float8_e4m3fn with scale = max|x| / 448 per piece.
+    Returns (uint8 codes of the cache's shape, fp32 [scale_c, scale_R])."""
+    sigma = torch.empty(2, device=device).uniform_(0.25, 4.0, generator=g)
+    x = cache.float()
+    x[..., :D_C] *= sigma[0]
+    x[..., D_C:] *= sigma[1]
+    amax = torch.stack([x[..., :D_C].abs().amax(), x[..., D_C:].abs().amax()]).clamp(min=1e-6)
+    scale = (amax / 448.0).to(torch.float32)
+    x[..., :D_C] /= scale[0]
+    x[..., D_C:] /= scale[1]
+    codes = x.clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale
+
+
 def mla_case(B, n_h=128, *, seqlens=None, lo=None, hi=None, seed=SEED_BASE,
-             device="cpu", spare_pages=0, max_blocks=None) -> MlaCase:
+             device="cpu", spare_pages=0, max_blocks=None, kv_dtype="bf16") -> MlaCase:
+    """An MLA decode problem; ``kv_dtype="fp8"`` turns the latent cache into
+    E4M3 codes (see mla_fp8_codes) drawn after every other input, so the
+    queries, lengths and block table are those of the bf16 case."""
     g = _gen(seed, device)
     if seqlens is None:
         sl = draw_seqlens(B, lo, hi, g, device)
@@ -218,7 +242,12 @@ def mla_case(B, n_h=128, *, seqlens=None, lo=None, hi=None, seed=SEED_BASE,
     bt, num_pages = shuffled_block_table(sl, g, device, spare_pages, max_blocks)
     cache = _randn_bf16((num_pages, PAGE, D_LATENT), g, device)
     scale = 1.0 / math.sqrt(128 + 64)
-    return MlaCase(q_abs, q_rope, cache, sl, bt, scale, {"num_pages": num_pages})
+    case = MlaCase(q_abs, q_rope, cache, sl, bt, scale, {"num_pages": num_pages})
+    if kv_dtype == "fp8":
+        case.cache, case.kv_scale = mla_fp8_codes(cache, g, device)
+    elif kv_dtype != "bf16":
+        raise ValueError(kv_dtype)
+    return case
 
 
 def mla_proj_case(B, n_h=128, *, seed=SEED_BASE, device="cpu"):
@@ -272,12 +301,17 @@ CONFIG_INDEX = {"C0": 0, "C1": 1, "C2-MHA": 2, "C2-MQA": 2, "C3": 3,
 def config_case(name: str, device="cpu", kv_dtype="bf16"):
     """The named workload with its seed (1000 + config index).  C2-MHA and
     C2-MQA draw the same q (the seed's first draw) and independent K/V.
-    ``kv_dtype="fp8"`` (GQA workloads) turns the cache into E4M3 codes."""
+    ``kv_dtype="fp8"`` turns the cache into E4M3 codes (GQA: per-KV-head
+    scales; MLA: a c_kv and a k_R scale)."""
     c = CONFIGS[name]
     if kv_dtype != "bf16":
-        if c["kind"] != "gqa":
-            raise ValueError("an FP8 cache is built for the GQA workloads")
+        if kv_dtype != "fp8":
+            raise ValueError(kv_dtype)
         case = config_case(name, device)
+        if c["kind"] == "mla":
+            g = _gen(SEED_BASE + 500 + CONFIG_INDEX[name], device)
+            case.cache, case.kv_scale = mla_fp8_codes(case.cache, g, device)
+            return case
         g = _gen(SEED_BASE + 500 + CONFIG_INDEX[name], device)
         case.k, case.k_scale = fp8_codes(case.k, g, device)
         case.v, case.v_scale = fp8_codes(case.v, g, device)

@@ -17,6 +17,7 @@ from .attention import (  # noqa: F401
     append_rope_mla, append_rope_gqa, bf16_to_f64, f64_to_bf16_bits,
     bf16_bits_to_f64, gather_tokens, gather_slots, window_slots,
     e4m3_bits_to_f64, f64_to_e4m3_bits, dequant_e4m3, gqa_decode_fp8, E4M3_MAX,
+    dequant_mla_e4m3, mla_decode_absorbed_fp8,
     mla_prefill_expand, mla_prefill,
 )
 from . import closed_forms  # noqa: F401

@@ -140,6 +140,30 @@ def gqa_decode_fp8(q, k_codes, v_codes, k_scale, v_scale, seqlens, scale=None,
                       seqlens, scale, block_table, window)
 
 
+def dequant_mla_e4m3(codes, kv_scale) -> np.ndarray:
+    """Latent rows of an E4M3 MLA cache ([ARG] §六.3: FP8 halves the bytes
+    per cached element -- for DeepSeek-V3's 576-value row as for every
+    other cache -- with one scale per head or per token; the latent cache
+    has a single head).  Reading: one scale for the 512 c_kv values of every
+    row and one for its 64 k_R values (the two pieces of the row are
+    different tensors, [ARG] §四.2), value = E4M3(code) * scale.
+    codes uint8 [..., 576], kv_scale [c_kv scale, k_R scale]."""
+    v = e4m3_bits_to_f64(codes)
+    s = np.asarray(kv_scale, dtype=np.float64)
+    v[..., :512] *= s[0]
+    v[..., 512:] *= s[1]
+    return v
+
+
+def mla_decode_absorbed_fp8(q_abs, q_rope, codes, kv_scale, block_table, seqlens,
+                            scale=None):
+    """MLA absorbed decode over an E4M3 latent cache: the plain absorbed
+    decode of the dequantised rows ([ARG] §六.3: quantisation changes the
+    bytes per element, not the attention)."""
+    return mla_decode_absorbed(q_abs, q_rope, dequant_mla_e4m3(codes, kv_scale),
+                               block_table, seqlens, scale)
+
+
 # ----------------------------------------------------------------------------
 # softmax attention of one query block over one key/value sequence
 # ----------------------------------------------------------------------------
@@ -435,20 +459,34 @@ def rope_rotate(x: np.ndarray, pos, theta: float = 10000.0) -> np.ndarray:
 
 
 def append_rope_mla(cache_bits, block_table, seqlens, c_kv_bits, kr_bits,
-                    theta=10000.0):
+                    theta=10000.0, kv_scale=None):
     """Write one new token per sequence into the paged latent cache
     ([ARG] §四.2: c_kv is cached as is, k_R is cached already rotated;
-    [KVC-LLM] §2.2: the cache grows by one row).  All arrays are bf16 bit
+    [KVC-LLM] §2.2: the cache grows by one row).  Inputs are bf16 bit
     patterns (uint16).  Slot: pos = seqlens[b], page block_table[b, pos//64],
-    row pos % 64.  Returns a new cache array."""
+    row pos % 64.  Returns a new cache array.
+
+    bf16 cache (kv_scale None): bf16 bit patterns in and out.  E4M3 cache
+    (kv_scale = [c_kv scale, k_R scale], [ARG] §六.3; uint8 codes): c_kv code
+    = E4M3(c_kv / scale_c) taken from the binary32 quotient (the precision
+    the kernel divides in, so these codes are exact), k_R code =
+    E4M3(RoPE(k_R) / scale_R) from the binary64 rotation (within one code of
+    the kernel's binary32 rotation)."""
     out = np.array(cache_bits, copy=True)
+    fp8 = kv_scale is not None
     for b in range(len(seqlens)):
         pos = int(seqlens[b])
         page = int(block_table[b, pos // PAGE])
         row = pos % PAGE
-        out[page, row, :512] = c_kv_bits[b]
         rot = rope_rotate(bf16_bits_to_f64(kr_bits[b]), pos, theta)
-        out[page, row, 512:] = f64_to_bf16_bits(rot)
+        if fp8:
+            s32 = np.asarray(kv_scale, np.float32)
+            cq = bf16_bits_to_f64(c_kv_bits[b]).astype(np.float32) / s32[0]
+            out[page, row, :512] = f64_to_e4m3_bits(cq.astype(np.float64))
+            out[page, row, 512:] = f64_to_e4m3_bits(rot / np.float64(s32[1]))
+        else:
+            out[page, row, :512] = c_kv_bits[b]
+            out[page, row, 512:] = f64_to_bf16_bits(rot)
     return out
 
 

@@ -538,6 +538,93 @@ def test_fp8_append_codes():
         np.testing.assert_array_equal(V2[b, :, sl[b]], ref)
 
 
+def test_dequant_mla_splits_the_row():
+    """The latent row's first 512 values take the c_kv scale, its last 64
+    the k_R scale."""
+    codes = np.full((2, 3, 576), 0x38, np.uint8)            # every value 1.0
+    codes[0, 0, 511] = 0xC0                                 # -2.0
+    v = oracle.dequant_mla_e4m3(codes, [0.5, 4.0])
+    assert np.all(v[..., 512:] == 4.0)
+    assert v[0, 0, 511] == -1.0
+    assert np.all(np.delete(v[..., :512].reshape(-1), 511) == 0.5)
+
+
+def _mla_codes(shape):
+    c = RNG.integers(0, 256, shape).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x3C                            # no NaN codes
+    return c
+
+
+def test_mla_fp8_decode_equals_decode_of_dequantised_bf16():
+    """With power-of-two scales every dequantised value is a bf16 number, so
+    the FP8 MLA decode must equal the (pinned) bf16 absorbed decode of the
+    same rows; swapping the c_kv and k_R scales must not."""
+    case = kvgen.mla_case(2, 4, seqlens=[70, 9], seed=31)
+    codes = _mla_codes(case.cache.shape) & 0xBF               # exponent field <= 7
+    ks = np.array([2.0 ** -3, 2.0 ** 1])
+    qa, qr = oracle.bf16_to_f64(case.q_abs), oracle.bf16_to_f64(case.q_rope)
+    bt, sl = case.block_table.numpy(), case.seqlens.numpy()
+    out, lse = oracle.mla_decode_absorbed_fp8(qa, qr, codes, ks, bt, sl)
+    rows = oracle.e4m3_bits_to_f64(codes)
+    rows[..., :512] *= ks[0]
+    rows[..., 512:] *= ks[1]
+    assert np.array_equal(oracle.bf16_bits_to_f64(oracle.f64_to_bf16_bits(rows)), rows)
+    out2, lse2 = oracle.mla_decode_absorbed(qa, qr, rows, bt, sl)
+    np.testing.assert_array_equal(out, out2)
+    np.testing.assert_array_equal(lse, lse2)
+    bad, _ = oracle.mla_decode_absorbed_fp8(qa, qr, codes, ks[::-1], bt, sl)
+    assert not np.allclose(bad, out, atol=1e-3)
+
+
+def test_mla_fp8_scale_homogeneity():
+    """Scaling the whole cache row by s is the same as scaling both query
+    pieces by s (scores) and the latent output by s (values): with scales
+    (s_c, s_R), out = s_c * out(scales 1, q_abs * s_c, q_rope * s_R) and the
+    lse is unchanged.  A scale missing on the values, or applied to the
+    wrong piece of the row, breaks it."""
+    case = kvgen.mla_case(2, 4, seqlens=[130, 64], seed=32)
+    codes = _mla_codes(case.cache.shape)
+    qa, qr = oracle.bf16_to_f64(case.q_abs), oracle.bf16_to_f64(case.q_rope)
+    bt, sl = case.block_table.numpy(), case.seqlens.numpy()
+    sc, sr = 0.0125, 0.07
+    out, lse = oracle.mla_decode_absorbed_fp8(qa, qr, codes, [sc, sr], bt, sl)
+    out1, lse1 = oracle.mla_decode_absorbed_fp8(qa * sc, qr * sr, codes, [1.0, 1.0], bt, sl)
+    np.testing.assert_allclose(out, sc * out1, rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(lse, lse1, rtol=1e-12, atol=1e-12)
+    assert np.abs(out).max() > 1e-3
+
+
+def test_fp8_mla_append_codes():
+    """Quantising MLA append: the row lands at the slot of pos = seqlens[b];
+    c_kv codes equal the library cast of the binary32 quotient c_kv /
+    scale_c; k_R codes are the nearest codes to RoPE(k_R) / scale_R (half a
+    code step); nothing else changes."""
+    sl = np.array([0, 63, 64, 200])
+    case = kvgen.mla_case(4, 2, seqlens=[1, 64, 65, 201], seed=33, spare_pages=2,
+                          kv_dtype="fp8")
+    codes = case.cache.numpy()
+    bt = case.block_table.numpy()
+    ckv, kr = kvgen.append_inputs_mla(4, seed=34)
+    cb = ckv.view(torch.int16).numpy().view(np.uint16)
+    kb = kr.view(torch.int16).numpy().view(np.uint16)
+    ks = np.array([0.02, 0.011], np.float32)
+    new = oracle.append_rope_mla(codes, bt, sl, cb, kb, kv_scale=ks)
+    changed = np.argwhere(np.any(new != codes, axis=2))
+    expect = {(int(bt[b, sl[b] // 64]), int(sl[b] % 64)) for b in range(4)}
+    assert {tuple(x) for x in changed} <= expect
+    mags = oracle.e4m3_bits_to_f64(np.arange(0x7F))
+    for b in range(4):
+        page, row = bt[b, sl[b] // 64], sl[b] % 64
+        quot = torch.from_numpy(ckv[b].float().numpy() / ks[0])
+        np.testing.assert_array_equal(new[page, row, :512],
+                                      quot.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+        rot = oracle.rope_rotate(oracle.bf16_bits_to_f64(kb[b]), float(sl[b])) / np.float64(ks[1])
+        got = oracle.e4m3_bits_to_f64(new[page, row, 512:])
+        hi = np.searchsorted(mags, np.abs(rot))
+        gap = mags[np.minimum(hi, 126)] - mags[np.maximum(hi - 1, 0)]
+        assert np.all(np.abs(got - rot) <= gap / 2 + 1e-15)
+
+
 # ---------------------------------------------------------------- sliding window
 
 def test_window_matches_printed_mask():

@@ -77,7 +77,8 @@ def parse():
     ap.add_argument("--config", default="C4", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="kvdec", choices=["kvdec", "reference"])
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8"],
-                    help="GQA cache element: bf16, or E4M3 bytes with per-KV-head scales")
+                    help="cache element: bf16, or E4M3 bytes (GQA: per-KV-head scales; "
+                         "MLA: a c_kv and a k_R scale)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--quick", action="store_true",
                     help="profiling runs: no CPU baseline, no e2e leg, no clock hold")
@@ -115,13 +116,15 @@ def gqa_append_bytes(case):
 
 
 def mla_bytes(case, out_elem=4):
-    """Per cached token 576 bf16 values (1152 B), plus q (576 per head),
-    out (512 per head), lse, seqlens and block table once."""
+    """Per cached token 576 values (1152 B in bf16, 576 B as E4M3 codes),
+    plus q (576 per head), out (512 per head), lse, seqlens, block table
+    and the two E4M3 scales once."""
     sl = case.seqlens.double().sum().item()
     kv = sl * 576 * case.cache.element_size()
     q = case.B * case.n_h * 576 * 2
     out = case.B * case.n_h * 512 * out_elem + case.B * case.n_h * 4
-    return kv + q + out + case.B * 4 + case.block_table.numel() * 4, kv
+    scales = 0 if getattr(case, "kv_scale", None) is None else 8
+    return kv + q + out + case.B * 4 + case.block_table.numel() * 4 + scales, kv
 
 
 def mla_flops(case):
@@ -131,7 +134,8 @@ def mla_flops(case):
 
 
 def mla_append_bytes(case):
-    return case.B * (512 + 64) * 2 * 2 + case.B * 4
+    # c_kv and k_rope read (bf16); the row written (bf16 or E4M3); positions read
+    return case.B * (512 + 64) * (2 + case.cache.element_size()) + case.B * 4
 
 
 # ---------------------------------------------------------------- clocks
@@ -560,7 +564,7 @@ class Part:
         from decode_attention_kv_softmax_b300 import kvdec
         self.name = name
         self.mla = is_mla(name)
-        self.fp8 = (kv == "fp8") and not self.mla
+        self.fp8 = kv == "fp8"
         self.lib = lib
         self.kernel = "mla_decode_kernel" if self.mla else "gqa_decode_kernel"
         self.files = ["mla_decode.cu", "common.cuh", "schedule.cuh", "tcgen05.cuh"] if self.mla else \
@@ -575,7 +579,10 @@ class Part:
             if rep > 0:   # an independent draw of the same workload (new cache values)
                 g = torch.Generator(device=dev)
                 g.manual_seed(7777 + 101 * rep + rank)
-                if self.mla:
+                if self.mla and self.fp8:
+                    x = torch.randn(case.cache.shape, generator=g, device=dev).to(torch.bfloat16)
+                    case.cache.copy_(kvgen.mla_fp8_codes(x, g, dev)[0])
+                elif self.mla:
                     case.cache.copy_(torch.randn(case.cache.shape, generator=g, device=dev).to(torch.bfloat16))
                 elif self.fp8:
                     case.k.copy_(kvgen.fp8_codes(torch.randn(case.k.shape, generator=g, device=dev), g, dev)[0])
@@ -603,7 +610,8 @@ class Part:
             out = torch.empty((B, case.n_h, 512), dtype=torch.float32, device=dev)
             lse = torch.empty((B, case.n_h), dtype=torch.float32, device=dev)
             p = kvdec.mla_params(case.q_abs, case.q_rope, case.cache, case.block_table,
-                                 case.seqlens, case.scale, out, lse, None, 0)
+                                 case.seqlens, case.scale, out, lse, None, 0,
+                                 kv_scale=getattr(case, "kv_scale", None))
             need = lib.kvdec_mla_workspace_bytes(ctypes.byref(p))
             wsb = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
             p.workspace, p.workspace_bytes = kvdec._ptr(wsb), wsb.numel()
@@ -613,6 +621,9 @@ class Part:
             ap.num_pages, ap.max_blocks = case.cache.shape[0], case.block_table.shape[1]
             ap.rope_theta = 10000.0
             ap.c_kv, ap.k_rope, ap.cache = kvdec._ptr(ckv), kvdec._ptr(kr), kvdec._ptr(case.cache)
+            if self.fp8:
+                ap.kv_format = kvdec.KV_FP8_E4M3
+                ap.k_scale = kvdec._ptr(case.kv_scale)
             return dict(case=case, new=(ckv, kr), q=(case.q_abs, case.q_rope), pos=pos, out=out,
                         lse=lse, ws=wsb, p=p, ap=ap, decode=lib.kvdec_mla_decode_absorbed)
         k_new, v_new = kvgen.append_inputs_gqa(B, case.n_kv, case.d, seed=55 + rep, device=dev)
@@ -858,7 +869,9 @@ def main():
             t_hbm = dec_alg / (hbm_peak * 1e9)
             t_tc = part.flops / (bf16_peak * 1e12)
             r["tensor"] = {"achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
-                           "peak_source": f"{peak_src} bf16_tflops (cuBLAS GEMM, burst)",
+                           "peak_source": f"{peak_src} bf16_tflops (cuBLAS GEMM, burst)" +
+                           ("; the E4M3 cache's MMAs run in f16, whose nominal dense rate equals "
+                            "bf16's (ratio 1)" if part.fp8 else ""),
                            "algorithmic_flops_per_launch": part.flops}
             r["binding"] = "hbm" if t_hbm >= t_tc else "tensor"
             r["frac_of_binding"] = max(t_hbm, t_tc) / (mean_us * 1e-6)
@@ -970,7 +983,8 @@ def main():
            "l2": "; ".join(f"{p.name}: {p.l2_note(l2)}" for p in parts),
            "kv_bytes_per_step": sum(p.dec_bytes[0][1] for p in parts),
            "step": " + ".join(f"{p.name}: append_rope + decode (fused split merge)" for p in parts),
-           "kv_cache": "GQA E4M3 bytes with per-KV-head fp32 scales" if args.kv == "fp8" else "bf16",
+           "kv_cache": ("E4M3 bytes (GQA: per-KV-head fp32 scales; MLA: c_kv and k_R fp32 scales)"
+                        if args.kv == "fp8" else "bf16"),
            "parallelism": f"replicas x{ws}"}
     line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,

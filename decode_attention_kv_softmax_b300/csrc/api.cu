@@ -280,11 +280,14 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
         return fail(KVDEC_ERR_INVALID_ARG, "batch %d outside [1, %d]", p->batch, kvdec::max_batch_mla());
     if (p->num_pages < 1 || p->max_blocks < 1)
         return fail(KVDEC_ERR_INVALID_ARG, "num_pages and max_blocks must be >= 1");
+    if (p->kv_format != KVDEC_KV_BF16 && p->kv_format != KVDEC_KV_FP8_E4M3)
+        return fail(KVDEC_ERR_INVALID_ARG, "kv_format %d", p->kv_format);
+    const bool fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
     DeviceInfo di;
     int dev;
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
-    int pairs = cached_occupancy(std::make_tuple(dev, 1, 0, 0, p->batch),
-                                 [&] { return kvdec::max_pairs_mla(p->batch); });
+    int pairs = cached_occupancy(std::make_tuple(dev, 1, fp8 ? 1 : 0, 0, p->batch),
+                                 [&] { return kvdec::max_pairs_mla(p->batch, fp8); });
     if (pairs < 1) return fail(KVDEC_ERR_CUDA, "MLA kernel clusters do not fit on this device");
     if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
     pl.pairs = pairs;
@@ -461,9 +464,22 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     const uint64_t rows = (uint64_t)p->num_pages * KVDEC_PAGE_SIZE;
     if (rows >= 0x7fffffffull || (uint64_t)p->max_blocks * KVDEC_PAGE_SIZE >= 0x7fffffffull)
         return fail(KVDEC_ERR_UNSUPPORTED, "cache too large (rows >= 2^31)");
+    const bool fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
+    if (fp8 && (!p->kv_scale || !aligned(p->kv_scale, 4)))
+        return fail(KVDEC_ERR_INVALID_ARG, "an E4M3 latent cache needs kv_scale = fp32 [c_kv scale, k_R scale]");
     kvdec::MlaMaps maps;
-    if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
-    if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+    if (fp8) {
+        // 64 c_kv codes or 32 k_R codes of 64 tokens per box, unswizzled
+        if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8)))
+            return st;
+        if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_DATA_TYPE_UINT8)))
+            return st;
+    } else {
+        if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+        if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+    }
     // stores of O / l, 32 rows x 32 fp32 columns per box: partials, and out when it is fp32
     if ((st = encode_2d(&maps.part, static_cast<uint8_t*>(p->workspace) + pl.off_o, 2 * (uint64_t)pl.pairs * 128, 512,
                         2048, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
@@ -497,6 +513,8 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     a.min_tiles = 4;
     a.seg_cost = kvdec::kMlaSeqStartCost;
     a.timeout_ns = kvdec::kDefaultTimeoutNs;
+    a.fp8 = fp8 ? 1 : 0;
+    a.kv_scale = p->kv_scale;
     cudaError_t e = kvdec::launch_mla(maps, a, pl.pairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
     return KVDEC_OK;
@@ -673,13 +691,18 @@ kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream) {
     if (p->block_table && (p->num_pages < 1 || p->max_blocks < 1))
         return fail(KVDEC_ERR_INVALID_ARG, "paged append needs num_pages >= 1 and max_blocks >= 1");
     if (p->mode == KVDEC_APPEND_MLA) {
-        if (p->kv_format != KVDEC_KV_BF16 || p->window != 0)
-            return fail(KVDEC_ERR_UNSUPPORTED, "MLA append takes neither kv_format nor window");
+        if (p->window != 0) return fail(KVDEC_ERR_UNSUPPORTED, "MLA append takes no window");
+        if (p->kv_format != KVDEC_KV_BF16 && p->kv_format != KVDEC_KV_FP8_E4M3)
+            return fail(KVDEC_ERR_INVALID_ARG, "kv_format %d", p->kv_format);
         if (!p->block_table || !p->c_kv || !p->k_rope || !p->cache)
             return fail(KVDEC_ERR_INVALID_ARG, "MLA append needs block_table, c_kv, k_rope and cache");
         if (!aligned(p->c_kv, 16) || !aligned(p->cache, 16) || !aligned(p->k_rope, 4))
             return fail(KVDEC_ERR_INVALID_ARG, "c_kv and cache must be 16-byte aligned");
         a.mode = 0;
+        a.fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
+        if (a.fp8 && (!p->k_scale || !aligned(p->k_scale, 4)))
+            return fail(KVDEC_ERR_INVALID_ARG, "an E4M3 latent cache needs k_scale = fp32 [c_kv scale, k_R scale]");
+        a.k_scale = p->k_scale;
         a.c_kv = static_cast<const __nv_bfloat16*>(p->c_kv);
         a.k_rope = static_cast<const __nv_bfloat16*>(p->k_rope);
         a.cache = static_cast<__nv_bfloat16*>(p->cache);

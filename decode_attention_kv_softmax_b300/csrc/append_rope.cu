@@ -12,9 +12,10 @@
 // binary32, and the result is rounded once to bf16 (nearest-even).  The kernel moves a few KB per call: it is launch-latency
 // bound, so it is written for simplicity, one CTA per (sequence, head).
 //
-// GQA options: an FP8 cache ([ARG] §六.3) stores E4M3(x / scale[kv head])
-// (nearest-even, saturating at 448; the quotient is the correctly rounded
-// binary32 one), and a sliding window of w tokens ([ARG] §五.3) writes the
+// Options: an FP8 cache ([ARG] §六.3) stores E4M3(x / scale) (nearest-even,
+// saturating at 448; the quotient is the correctly rounded binary32 one),
+// with one scale per KV head (GQA) or one for c_kv and one for k_R (MLA);
+// and (GQA) a sliding window of w tokens ([ARG] §五.3) writes the
 // ring slot pos mod w while the rotation keeps the position pos.
 #include <cuda_fp8.h>
 
@@ -67,6 +68,27 @@ __global__ void __launch_bounds__(64) append_rope_kernel(const AppendArgs a) {
         }
     }
     const int slot = pos % KVDEC_PAGE_SIZE;
+    if (a.mode == 0 && a.fp8) {
+        // E4M3 latent row: [E4M3(c_kv / s_c) ; E4M3(RoPE(k_rope) / s_R)], s = k_scale[0..1]
+        uint8_t* row = reinterpret_cast<uint8_t*>(a.cache) +
+                       ((size_t)page * KVDEC_PAGE_SIZE + slot) * (KVDEC_MLA_DC + KVDEC_MLA_DR);
+        const float sc = __ldg(a.k_scale), sr = __ldg(a.k_scale + 1);
+        const uint4 x = __ldg(reinterpret_cast<const uint4*>(a.c_kv + (size_t)b * KVDEC_MLA_DC) + t);
+        const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+        uint32_t c[2] = {0u, 0u};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {   // 8 values of 64 threads = 512
+            const uint32_t bits = (i & 1) ? (w[i >> 1] & 0xffff0000u) : (w[i >> 1] << 16);
+            c[i >> 2] |= (uint32_t)to_e4m3(__fdiv_rn(__uint_as_float(bits), sc)) << (8 * (i & 3));
+        }
+        *reinterpret_cast<uint2*>(row + 8 * t) = make_uint2(c[0], c[1]);
+        if (t < KVDEC_MLA_DR / 2) {
+            const float2 r = rope_pair_f32(a.k_rope + (size_t)b * KVDEC_MLA_DR, t, pos, a.inv_freq);
+            row[KVDEC_MLA_DC + 2 * t] = to_e4m3(__fdiv_rn(r.x, sr));
+            row[KVDEC_MLA_DC + 2 * t + 1] = to_e4m3(__fdiv_rn(r.y, sr));
+        }
+        return;
+    }
     if (a.mode == 0) {
         // MLA latent row: [c_kv (512, copied) ; RoPE(k_rope) (64)]
         __nv_bfloat16* row = a.cache + ((size_t)page * KVDEC_PAGE_SIZE + slot) * (KVDEC_MLA_DC + KVDEC_MLA_DR);

@@ -59,15 +59,19 @@ struct AppendArgs {
     void* v;
     int n_kv, d, cap;
     uint32_t* err;
-    int fp8;             // GQA: E4M3 cache with per-KV-head scales
+    int fp8;             // E4M3 cache (GQA: per-KV-head scales; MLA: k_scale = [c_kv, k_R])
     int window;          // GQA: > 0 ring cache of `window` slots
     const float* k_scale;
     const float* v_scale;
 };
 
 struct MlaMaps {
-    CUtensorMap c128;  // cache [pages*64, 576], box 64 x 64, 128-byte swizzle
-    CUtensorMap c64;   // cache [pages*64, 576], box 32 x 64, 64-byte swizzle
+    // bf16 cache [pages*64, 576]: c128 box 64 x 64 with the 128-byte swizzle,
+    // c64 box 32 x 64 with the 64-byte swizzle.  E4M3 cache (bytes): c128
+    // box 64 x 64 (a quarter of a CTA's c_kv half), c64 box 32 x 64 (its k_R
+    // half), no swizzle.
+    CUtensorMap c128;
+    CUtensorMap c64;
     CUtensorMap part;  // partial O [2*pairs*128, 512] fp32, box 32 x 32, 128-byte swizzle (stores)
     CUtensorMap outf;  // out [B*128, 512] fp32, same box (stores; unused for bf16 out)
 };
@@ -90,6 +94,8 @@ struct MlaArgs {
     int min_tiles;
     int seg_cost;                   // start cost of a sequence, in pages (schedule.cuh)
     uint64_t timeout_ns;
+    int fp8;                        // E4M3 latent cache
+    const float* kv_scale;          // E4M3: fp32 [c_kv scale, k_R scale]
 };
 
 // Start cost of a sequence in the MLA decode schedule, in pages: loading a
@@ -143,7 +149,7 @@ struct MlaExpandArgs {
     uint64_t timeout_ns;
 };
 cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs& a, cudaStream_t st);
-int max_pairs_mla(int B);
+int max_pairs_mla(int B, bool fp8);
 int max_batch_mla();   // largest batch whose tile table fits in shared memory
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -16,7 +16,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvdec.so")
 
-ABI_VERSION = 2
+ABI_VERSION = 3
 F32, BF16 = 0, 1
 KV_BF16, KV_FP8_E4M3 = 0, 1
 APPEND_MLA, APPEND_GQA = 0, 1
@@ -43,7 +43,8 @@ class MlaParams(ctypes.Structure):
                 ("num_heads", c_int32), ("num_pages", c_int32), ("max_blocks", c_int32),
                 ("scale", c_float), ("out", c_void_p), ("out_dtype", c_int32),
                 ("lse", c_void_p), ("workspace", c_void_p), ("workspace_bytes", c_size_t),
-                ("error_flag", c_void_p), ("max_ctas", c_int32), ("reserved", c_int32)]
+                ("error_flag", c_void_p), ("max_ctas", c_int32), ("kv_format", c_int32),
+                ("kv_scale", c_void_p)]
 
 
 class AppendParams(ctypes.Structure):
@@ -336,9 +337,27 @@ def gqa_decode_noalloc(q, k, v, seqlens, block_table=None, scale=None,
 
 # ---------------------------------------------------------------- MLA
 
+def _mla_kv_format(cache, kv_scale, dev) -> int:
+    """KV_BF16 for a bf16 latent cache; KV_FP8_E4M3 for E4M3 bytes (uint8 or
+    float8_e4m3fn) with fp32 [c_kv scale, k_R scale] on the same device."""
+    if cache.dtype == torch.bfloat16:
+        return KV_BF16
+    if cache.dtype not in _FP8_DTYPES:
+        raise TypeError(f"cache must be bf16 or E4M3 bytes, got {cache.dtype}")
+    if kv_scale is None:
+        raise ValueError("an FP8 latent cache needs kv_scale")
+    _need(kv_scale, "kv_scale", torch.float32, dev)
+    if kv_scale.numel() != 2:
+        raise ValueError("kv_scale must hold [c_kv scale, k_R scale]")
+    return KV_FP8_E4M3
+
+
 def mla_params(q_abs, q_rope, cache, block_table, seqlens, scale=None, out=None, lse=None,
-               error_flag=None, max_ctas=0):
+               error_flag=None, max_ctas=0, kv_scale=None):
     p = MlaParams()
+    if cache.dtype in _FP8_DTYPES:
+        p.kv_format = KV_FP8_E4M3
+        p.kv_scale = _ptr(kv_scale)
     B, H, _ = q_abs.shape
     p.q_absorbed, p.q_rope, p.cache = _ptr(q_abs), _ptr(q_rope), _ptr(cache)
     p.block_table, p.seqlens = _ptr(block_table), _ptr(seqlens)
@@ -355,20 +374,24 @@ def mla_params(q_abs, q_rope, cache, block_table, seqlens, scale=None, out=None,
 
 def mla_decode_absorbed(q_abs, q_rope, cache, block_table, seqlens, scale=None,
                         out_dtype=torch.float32, out=None, return_lse=True, error_flag=None,
-                        max_ctas=0, workspace=None, stream=None):
-    """MLA absorbed decode.  q_abs [B,128,512], q_rope [B,128,64], cache
-    [pages,64,576] (all bf16); block_table [B,max_blocks] and seqlens [B]
-    int32.  Returns (out [B,128,512] latent, lse [B,128] or None)."""
+                        max_ctas=0, workspace=None, stream=None, kv_scale=None):
+    """MLA absorbed decode.  q_abs [B,128,512], q_rope [B,128,64] bf16; cache
+    [pages,64,576] bf16, or E4M3 bytes (uint8 / float8_e4m3fn) with kv_scale
+    = fp32 [c_kv scale, k_R scale]; block_table [B,max_blocks] and seqlens
+    [B] int32.  Returns (out [B,128,512] latent, lse [B,128] or None)."""
     lib = load()
     dev = q_abs.device
-    for t, n in [(q_abs, "q_abs"), (q_rope, "q_rope"), (cache, "cache")]:
+    for t, n in [(q_abs, "q_abs"), (q_rope, "q_rope")]:
         _need(t, n, torch.bfloat16, dev)
+    _need(cache, "cache", cache.dtype, dev)
+    _mla_kv_format(cache, kv_scale, dev)
     _need(block_table, "block_table", torch.int32, dev)
     _need(seqlens, "seqlens", torch.int32, dev)
     if out is None:
         out = torch.empty(q_abs.shape, dtype=out_dtype, device=dev)
     lse = torch.empty(q_abs.shape[:2], dtype=torch.float32, device=dev) if return_lse else None
-    p = mla_params(q_abs, q_rope, cache, block_table, seqlens, scale, out, lse, error_flag, max_ctas)
+    p = mla_params(q_abs, q_rope, cache, block_table, seqlens, scale, out, lse, error_flag, max_ctas,
+                   kv_scale)
     need = lib.kvdec_mla_workspace_bytes(ctypes.byref(p))
     if need == 0:
         raise KvdecError("kvdec_mla_decode_absorbed: " + lib.kvdec_last_error().decode())
@@ -384,17 +407,24 @@ def mla_decode_absorbed(q_abs, q_rope, cache, block_table, seqlens, scale=None,
 # ---------------------------------------------------------------- append
 
 def append_rope_mla(cache, block_table, seqlens, c_kv, k_rope, rope_theta=10000.0,
-                    error_flag=None, stream=None):
+                    error_flag=None, stream=None, kv_scale=None):
     """Write [c_kv ; RoPE_pos(k_rope)] at slot seqlens[b] of the paged latent
-    cache (in place).  The caller increments seqlens afterwards."""
+    cache (in place).  The caller increments seqlens afterwards.  An E4M3
+    cache (uint8 / float8_e4m3fn) stores the codes of c_kv / kv_scale[0] and
+    RoPE(k_rope) / kv_scale[1]."""
     lib = load()
     dev = cache.device
-    for t, n in [(cache, "cache"), (c_kv, "c_kv"), (k_rope, "k_rope")]:
+    for t, n in [(c_kv, "c_kv"), (k_rope, "k_rope")]:
         _need(t, n, torch.bfloat16, dev)
+    _need(cache, "cache", cache.dtype, dev)
+    fmt = _mla_kv_format(cache, kv_scale, dev)
     _need(block_table, "block_table", torch.int32, dev)
     _need(seqlens, "seqlens", torch.int32, dev)
     p = AppendParams()
     p.mode = APPEND_MLA
+    p.kv_format = fmt
+    if fmt == KV_FP8_E4M3:
+        p.k_scale = _ptr(kv_scale)
     p.batch = c_kv.shape[0]
     p.seqlens, p.block_table = _ptr(seqlens), _ptr(block_table)
     p.num_pages, p.max_blocks = cache.shape[0], block_table.shape[1]

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define KVDEC_ABI_VERSION 2
+#define KVDEC_ABI_VERSION 3
 #define KVDEC_PAGE_SIZE 64      /* tokens per KV page (block) */
 #define KVDEC_MLA_DC 512        /* MLA latent width d_c */
 #define KVDEC_MLA_DR 64         /* MLA decoupled rope key width d_h^R */
@@ -62,12 +62,13 @@ typedef enum kvdec_status {
 
 typedef enum kvdec_dtype { KVDEC_F32 = 0, KVDEC_BF16 = 1 } kvdec_dtype;
 
-/* Element format of a GQA K/V cache ([ARG] §六.3: quantising the cache to
- * FP8 E4M3 halves the bytes per element, with one scale per head or per
- * token).  KVDEC_KV_FP8_E4M3: every K and V element is one E4M3 byte (the
- * format of "FP8 Formats for Deep Learning", Micikevicius et al. 2022), and
- * the value it stands for is E4M3(code) * scale[kv head], with one fp32 scale
- * per KV head for K and one for V. */
+/* Element format of a K/V cache ([ARG] §六.3: quantising the cache to FP8
+ * E4M3 halves the bytes per element, with one scale per head or per token).
+ * KVDEC_KV_FP8_E4M3: every cached element is one E4M3 byte (the format of
+ * "FP8 Formats for Deep Learning", Micikevicius et al. 2022), and the value
+ * it stands for is E4M3(code) * scale: for a GQA cache one fp32 scale per KV
+ * head for K and one for V; for the MLA latent cache one for the 512 c_kv
+ * values of every row and one for its 64 k_R values. */
 typedef enum kvdec_kv_format { KVDEC_KV_BF16 = 0, KVDEC_KV_FP8_E4M3 = 1 } kvdec_kv_format;
 
 /* ------------------------------------------------------------------------ */
@@ -195,6 +196,12 @@ kvdec_status kvdec_gqa_decode_noalloc(const kvdec_gqa_params* p, void* stream);
  *   cache bf16 [num_pages, 64, 576]; block_table int32 [batch, max_blocks]
  *   seqlens int32 [batch]; out [batch, num_heads, 512] F32 or BF16;
  *   lse fp32 [batch, num_heads] or NULL
+ * FP8 latent cache (kv_format = KVDEC_KV_FP8_E4M3): cache holds uint8 E4M3
+ *   codes [num_pages, 64, 576] (576 bytes a token); kv_scale is a device
+ *   array fp32 [2] (required): c_kv = E4M3(code[0:512]) * kv_scale[0],
+ *   k_R = E4M3(code[512:576]) * kv_scale[1].  The tensor cores take f16
+ *   operands on this path: q_absorbed * kv_scale[0] and q_rope * kv_scale[1]
+ *   are rounded to f16 (magnitudes must stay below 65504).
  * Supported: num_heads == 128 (tensor-core tile height) and
  * batch <= kvdec_mla_max_batch(): the kernel keeps a per-sequence tile table
  * in shared memory beside its cache stages, so a larger batch is rejected
@@ -219,7 +226,8 @@ typedef struct kvdec_mla_params {
     size_t workspace_bytes;
     uint32_t* error_flag;
     int32_t max_ctas;        /* 0 = one full wave of CTA pairs */
-    int32_t reserved;
+    int32_t kv_format;       /* kvdec_kv_format; 0 = bf16 */
+    const float* kv_scale;   /* FP8 only: fp32 [2] = {c_kv scale, k_R scale} */
 } kvdec_mla_params;
 
 size_t kvdec_mla_workspace_bytes(const kvdec_mla_params* p);
@@ -251,10 +259,15 @@ int32_t kvdec_mla_max_batch(void);
  *      exactly as in kvdec_gqa_decode.
  *   window = w > 0 (GQA only): the row goes to ring slot pos mod w (the
  *   rotation still uses pos), matching kvdec_gqa_decode's sliding window.
- *   kv_format = KVDEC_KV_FP8_E4M3 (GQA only, head_dim 128): K code =
+ *   kv_format = KVDEC_KV_FP8_E4M3 (GQA: head_dim 128): K code =
  *   E4M3(RoPE_pos(k_new) / k_scale[kv]) from the binary32 rotation, V code =
  *   E4M3(v_new / v_scale[kv]) from the correctly rounded binary32 quotient;
  *   nearest-even, magnitudes above 448 saturate to 448.
+ *   kv_format = KVDEC_KV_FP8_E4M3 (MLA): the cache holds uint8 codes
+ *   [num_pages, 64, 576] and k_scale is the fp32 [2] array {c_kv scale,
+ *   k_R scale} of kvdec_mla_decode_absorbed; c_kv codes = E4M3(c_kv /
+ *   k_scale[0]) from the correctly rounded binary32 quotient, k_R codes =
+ *   E4M3(RoPE_pos(k_rope) / k_scale[1]) from the binary32 rotation.
  * pos (or its ring slot) outside [0, capacity) or a bad page entry sets the
  * error bit and the row is skipped.
  */
@@ -284,8 +297,8 @@ typedef struct kvdec_append_params {
     uint32_t* error_flag;        /* optional */
     int32_t kv_format;           /* GQA: kvdec_kv_format; 0 = bf16 */
     int32_t window;              /* GQA: 0, or w > 0 for a ring cache of w slots */
-    const float* k_scale;        /* FP8: fp32 [num_kv_heads] */
-    const float* v_scale;        /* FP8: fp32 [num_kv_heads] */
+    const float* k_scale;        /* FP8: fp32 [num_kv_heads] (MLA: {c_kv, k_R} scales) */
+    const float* v_scale;        /* FP8 GQA: fp32 [num_kv_heads] */
 } kvdec_append_params;
 
 kvdec_status kvdec_append_rope(const kvdec_append_params* p, void* stream);

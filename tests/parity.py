@@ -142,18 +142,26 @@ def gqa_full_oracle(case):
 
 def mla_full_oracle(case):
     """Oracle latent output and lse of a whole MlaCase, one oracle call per
-    sequence on that sequence's pages (gathered in logical order)."""
+    sequence on that sequence's pages (gathered in logical order).  E4M3
+    caches (kv_scale set) go through the oracle's FP8 decode on the raw
+    codes."""
     sl = case.seqlens.to("cpu").numpy()
     bt = case.block_table.to("cpu").numpy()
+    fp8 = getattr(case, "kv_scale", None) is not None
+    ks = case.kv_scale.to("cpu").numpy() if fp8 else None
     out = np.zeros((case.B, case.n_h, 512))
     lse = np.zeros((case.B, case.n_h))
     for b in range(case.B):
         L = int(sl[b])
         npg = max((L + 63) // 64, 1)
         pages = torch.as_tensor(bt[b, :npg], dtype=torch.long, device=case.cache.device)
-        o, l = oracle.mla_decode_absorbed(f64(case.q_abs[b:b + 1]), f64(case.q_rope[b:b + 1]),
-                                          f64(case.cache[pages]), np.arange(npg)[None], [L],
-                                          case.scale)
+        qa, qr = f64(case.q_abs[b:b + 1]), f64(case.q_rope[b:b + 1])
+        if fp8:
+            o, l = oracle.mla_decode_absorbed_fp8(qa, qr, case.cache[pages].to("cpu").numpy(), ks,
+                                                  np.arange(npg)[None], [L], case.scale)
+        else:
+            o, l = oracle.mla_decode_absorbed(qa, qr, f64(case.cache[pages]), np.arange(npg)[None], [L],
+                                              case.scale)
         out[b], lse[b] = o[0], l[0]
     return out, lse
 

@@ -270,6 +270,9 @@ bool scale_ok(float s) { return s == 0.f || (s > 0.f && std::isfinite(s)); }
 struct MlaPlan {
     int pairs;
     size_t off_lse, off_o, bytes;
+    // E4M3 cache: the widened bf16 copy of the pages the call reads and its
+    // identity block table (mla_widen.cu)
+    size_t off_table, off_copy;
 };
 
 kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
@@ -282,12 +285,11 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
         return fail(KVDEC_ERR_INVALID_ARG, "num_pages and max_blocks must be >= 1");
     if (p->kv_format != KVDEC_KV_BF16 && p->kv_format != KVDEC_KV_FP8_E4M3)
         return fail(KVDEC_ERR_INVALID_ARG, "kv_format %d", p->kv_format);
-    const bool fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
     DeviceInfo di;
     int dev;
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
-    int pairs = cached_occupancy(std::make_tuple(dev, 1, fp8 ? 1 : 0, 0, p->batch),
-                                 [&] { return kvdec::max_pairs_mla(p->batch, fp8); });
+    int pairs = cached_occupancy(std::make_tuple(dev, 1, 0, 0, p->batch),
+                                 [&] { return kvdec::max_pairs_mla(p->batch); });
     if (pairs < 1) return fail(KVDEC_ERR_CUDA, "MLA kernel clusters do not fit on this device");
     if (p->max_ctas > 0) pairs = std::min(std::max(1, p->max_ctas / 2), 64 * pairs);
     pl.pairs = pairs;
@@ -295,6 +297,13 @@ kvdec_status plan_mla(const kvdec_mla_params* p, MlaPlan& pl) {
     pl.off_lse = round_up((size_t)p->batch * 2 * 4 * 8, 256);
     pl.off_o = pl.off_lse + round_up(2 * slots * 128 * 4, 256);
     pl.bytes = pl.off_o + slots * 128 * 512 * 4;
+    pl.off_table = pl.off_copy = 0;
+    if (p->kv_format == KVDEC_KV_FP8_E4M3) {
+        const size_t copy_pages = (size_t)p->batch * p->max_blocks;
+        pl.off_table = round_up(pl.bytes, 256);
+        pl.off_copy = round_up(pl.off_table + copy_pages * 4, 256);
+        pl.bytes = pl.off_copy + copy_pages * KVDEC_PAGE_SIZE * 576 * 2;
+    }
     return KVDEC_OK;
 }
 
@@ -464,22 +473,41 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     const uint64_t rows = (uint64_t)p->num_pages * KVDEC_PAGE_SIZE;
     if (rows >= 0x7fffffffull || (uint64_t)p->max_blocks * KVDEC_PAGE_SIZE >= 0x7fffffffull)
         return fail(KVDEC_ERR_UNSUPPORTED, "cache too large (rows >= 2^31)");
+    if (!scale_ok(p->scale)) return fail(KVDEC_ERR_INVALID_ARG, "scale %g (must be 0 or positive and finite)", (double)p->scale);
+    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+    // E4M3 cache: widen the pages this call reads into the workspace's bf16
+    // copy, then decode the copy through its identity block table
     const bool fp8 = p->kv_format == KVDEC_KV_FP8_E4M3;
-    if (fp8 && (!p->kv_scale || !aligned(p->kv_scale, 4)))
-        return fail(KVDEC_ERR_INVALID_ARG, "an E4M3 latent cache needs kv_scale = fp32 [c_kv scale, k_R scale]");
-    kvdec::MlaMaps maps;
+    const void* cache = p->cache;
+    const int32_t* block_table = p->block_table;
+    int num_pages = p->num_pages;
     if (fp8) {
-        // 64 c_kv codes or 32 k_R codes of 64 tokens per box, unswizzled
-        if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 576, 64, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8)))
-            return st;
-        if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 576, 32, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_DATA_TYPE_UINT8)))
-            return st;
-    } else {
-        if ((st = encode_2d(&maps.c128, p->cache, rows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
-        if ((st = encode_2d(&maps.c64, p->cache, rows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
+        if (!p->kv_scale || !aligned(p->kv_scale, 4))
+            return fail(KVDEC_ERR_INVALID_ARG, "an E4M3 latent cache needs kv_scale = fp32 [c_kv scale, k_R scale]");
+        const uint64_t copy_rows = (uint64_t)p->batch * p->max_blocks * KVDEC_PAGE_SIZE;
+        if (copy_rows >= 0x7fffffffull)
+            return fail(KVDEC_ERR_UNSUPPORTED, "batch * max_blocks * 64 >= 2^31 (split the call)");
+        kvdec::MlaWidenArgs w;
+        w.codes = static_cast<const uint8_t*>(p->cache);
+        w.block_table = p->block_table;
+        w.seqlens = p->seqlens;
+        w.kv_scale = p->kv_scale;
+        w.copy = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_copy);
+        w.copy_table = reinterpret_cast<int32_t*>(ws + pl.off_table);
+        w.B = p->batch;
+        w.num_pages = p->num_pages;
+        w.max_blocks = p->max_blocks;
+        w.err = p->error_flag;
+        cudaError_t e = kvdec::launch_mla_widen(w, static_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) return cuda_fail(e, "MLA widening launch");
+        cache = w.copy;
+        block_table = w.copy_table;
+        num_pages = p->batch * p->max_blocks;
     }
+    const uint64_t crows = (uint64_t)num_pages * KVDEC_PAGE_SIZE;
+    kvdec::MlaMaps maps;
+    if ((st = encode_2d(&maps.c128, cache, crows, 576, 1152, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))) return st;
+    if ((st = encode_2d(&maps.c64, cache, crows, 576, 1152, 32, 64, CU_TENSOR_MAP_SWIZZLE_64B))) return st;
     // stores of O / l, 32 rows x 32 fp32 columns per box: partials, and out when it is fp32
     if ((st = encode_2d(&maps.part, static_cast<uint8_t*>(p->workspace) + pl.off_o, 2 * (uint64_t)pl.pairs * 128, 512,
                         2048, 32, 32, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)))
@@ -493,28 +521,24 @@ kvdec_status kvdec_mla_decode_absorbed(const kvdec_mla_params* p, void* stream) 
     memset(&a, 0, sizeof(a));
     a.q_abs = static_cast<const __nv_bfloat16*>(p->q_absorbed);
     a.q_rope = static_cast<const __nv_bfloat16*>(p->q_rope);
-    a.block_table = p->block_table;
+    a.block_table = block_table;
     a.seqlens = p->seqlens;
     a.out = p->out;
     a.lse = p->lse;
-    uint8_t* ws = static_cast<uint8_t*>(p->workspace);
     a.counters = reinterpret_cast<unsigned long long*>(ws);
     a.part_lse = reinterpret_cast<float*>(ws + pl.off_lse);
     a.part_o = reinterpret_cast<float*>(ws + pl.off_o);
     a.epoch = next_epoch();
     a.err = p->error_flag;
     a.B = p->batch;
-    a.num_pages = p->num_pages;
+    a.num_pages = num_pages;
     a.max_blocks = p->max_blocks;
     a.out_bf16 = p->out_dtype == KVDEC_BF16;
-    if (!scale_ok(p->scale)) return fail(KVDEC_ERR_INVALID_ARG, "scale %g (must be 0 or positive and finite)", (double)p->scale);
     const double scale = p->scale != 0.f ? (double)p->scale : 1.0 / std::sqrt(192.0);
     a.scale_log2 = (float)(scale * 1.4426950408889634);
     a.min_tiles = 4;
     a.seg_cost = kvdec::kMlaSeqStartCost;
     a.timeout_ns = kvdec::kDefaultTimeoutNs;
-    a.fp8 = fp8 ? 1 : 0;
-    a.kv_scale = p->kv_scale;
     cudaError_t e = kvdec::launch_mla(maps, a, pl.pairs, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "MLA decode launch");
     return KVDEC_OK;

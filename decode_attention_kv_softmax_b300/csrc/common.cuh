@@ -365,12 +365,6 @@ KVDEC_DEVINL uint32_t bf16x2_to_f16x2(uint32_t u) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// bf16x2 times s, rounded once to f16x2 (nearest-even)
-KVDEC_DEVINL uint32_t bf16x2_scaled_to_f16x2(uint32_t u, float s) {
-    const __half2 h = __floats2half2_rn(__uint_as_float(u << 16) * s, __uint_as_float(u & 0xffff0000u) * s);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 // ---------------------------------------------------------------- numerics
 
 // 2^x on the special-function unit (ex2.approx: a PTX instruction).

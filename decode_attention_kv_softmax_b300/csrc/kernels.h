@@ -66,12 +66,8 @@ struct AppendArgs {
 };
 
 struct MlaMaps {
-    // bf16 cache [pages*64, 576]: c128 box 64 x 64 with the 128-byte swizzle,
-    // c64 box 32 x 64 with the 64-byte swizzle.  E4M3 cache (bytes): c128
-    // box 64 x 64 (a quarter of a CTA's c_kv half), c64 box 32 x 64 (its k_R
-    // half), no swizzle.
-    CUtensorMap c128;
-    CUtensorMap c64;
+    CUtensorMap c128;  // cache [pages*64, 576], box 64 x 64, 128-byte swizzle
+    CUtensorMap c64;   // cache [pages*64, 576], box 32 x 64, 64-byte swizzle
     CUtensorMap part;  // partial O [2*pairs*128, 512] fp32, box 32 x 32, 128-byte swizzle (stores)
     CUtensorMap outf;  // out [B*128, 512] fp32, same box (stores; unused for bf16 out)
 };
@@ -94,9 +90,23 @@ struct MlaArgs {
     int min_tiles;
     int seg_cost;                   // start cost of a sequence, in pages (schedule.cuh)
     uint64_t timeout_ns;
-    int fp8;                        // E4M3 latent cache
-    const float* kv_scale;          // E4M3: fp32 [c_kv scale, k_R scale]
 };
+
+// Widening of the pages an MLA decode reads from an E4M3 latent cache into a
+// bf16 copy laid out in logical order (mla_widen.cu): tile lt of sequence b
+// (lt < its page count) goes to copy page b * max_blocks + lt, and the copy's
+// block table is the identity on [B, max_blocks].
+struct MlaWidenArgs {
+    const uint8_t* codes;       // [num_pages, 64, 576] E4M3
+    const int32_t* block_table; // [B, max_blocks]
+    const int32_t* seqlens;     // [B]
+    const float* kv_scale;      // [c_kv scale, k_R scale]
+    __nv_bfloat16* copy;        // [B * max_blocks, 64, 576]
+    int32_t* copy_table;        // [B, max_blocks], identity
+    int B, num_pages, max_blocks;
+    uint32_t* err;
+};
+cudaError_t launch_mla_widen(const MlaWidenArgs& a, cudaStream_t st);
 
 // Start cost of a sequence in the MLA decode schedule, in pages: loading a
 // new Q into TMEM and flushing O takes about as long as this many pages.
@@ -149,7 +159,7 @@ struct MlaExpandArgs {
     uint64_t timeout_ns;
 };
 cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs& a, cudaStream_t st);
-int max_pairs_mla(int B, bool fp8);
+int max_pairs_mla(int B);
 int max_batch_mla();   // largest batch whose tile table fits in shared memory
 
 cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,

@@ -42,20 +42,6 @@
 // all pages; sequences cut across pairs leave normalised partials, merged by
 // log-sum-exp ([ARG] §五.2) by the pair whose piece arrives last, once it has
 // finished its pages.
-//
-// E4M3 latent cache ([ARG] §六.3: FP8 halves the bytes per cached element;
-// F8 = true).  Four more warps (one per SM sub-partition) widen each page
-// in shared memory: the TMA stages a CTA's 288 codes per token (18 KB a
-// page) inside the stage, each box's codes in the upper half of that box,
-// and the converters rewrite the stage as the f16 page the MMAs read, in the
-// same layout as a bf16 page (every E4M3 value is an f16 number).  With 15
-// warps a CTA gets 128 registers a thread (4 warps share a sub-partition's
-// register file).
-// The MMAs then take f16 operands: Q_r is loaded pre-multiplied by the
-// scales (q_abs by the c_kv scale, q_rope by the k_R scale), so S needs no
-// extra work, and the c_kv scale multiplies O at the flush.  P goes to f16
-// scaled by 2^7 (one subtraction folded into the exponent), which keeps
-// probabilities down to 2^-21 of the reference max normal in f16.
 #include "common.cuh"
 #include "kernels.h"
 #include "schedule.cuh"
@@ -72,23 +58,14 @@ constexpr int kQRBytes = kHeads * 64;           // q_rope [128 x 32] bf16, K-maj
 constexpr int kHandBytes = 2 * 2 * kHeads * 8;  // hand-off: [2 groups][2][128] (m, l)
 constexpr int kSoftWarps = 8;                   // two groups of four
 constexpr int kGroupWarps = 4;
-// + S issuer, TMA producer, PV issuer (+ four E4M3 converters, one per SMSP)
-constexpr int kConvWarps = 4;
-template <bool F8> constexpr int threads() { return 32 * (kSoftWarps + 3 + (F8 ? kConvWarps : 0)); }
-// E4M3 page staged by the TMA inside the stage it widens into: the codes of
-// c_kv box c ([64 tokens][64]) in the upper half of box c's 8 KB, the k_R
-// codes ([64][32]) in the upper half of the rope box
-constexpr int kF8BoxOff = 4096;
-constexpr int kF8RopeOff = 32768 + 2048;
-constexpr int kF8Bytes = 4 * 4096 + 2048;
-constexpr float kPShift = 7.f;                  // E4M3 path: P = 2^7 p in f16
+constexpr int kThreads = 32 * (kSoftWarps + 3);   // + S issuer, TMA producer, PV issuer
 enum {
     B_Q_FULL, B_S_FULL, B_S_FREE = B_S_FULL + 2, B_P_FULL = B_S_FREE + 2, B_PV_DONE = B_P_FULL + 2,
     B_O_FREE = B_PV_DONE + 2, B_RECV_FULL, B_RECV_EMPTY,
     B_HAND,                                                                    // [4 quadrants][2 groups][2]
     B_DONE = B_HAND + 16, B_KV = B_DONE + 1                                    // then full[NS], empty[NS]
 };
-template <int NS, int PB, bool F8>
+template <int NS, int PB>
 struct Layout {
     static constexpr int kOffKV = 0;
     static constexpr int kOffRecv = NS * kStageBytes;
@@ -96,14 +73,13 @@ struct Layout {
     static constexpr int kOffQR = kOffP + PB * kPBytes;
     static constexpr int kOffHand = kOffQR + kQRBytes;
     static constexpr int kOffBars = kOffHand + kHandBytes;
-    static constexpr int kBars = B_KV + (F8 ? 3 : 2) * NS;   // E4M3: + codes_full[NS]
+    static constexpr int kBars = B_KV + 2 * NS;
     static constexpr int kOffMisc = kOffBars + ((kBars * 8 + 15) & ~15);   // [0] TMEM base, [1] abort word
     static constexpr int kOffPend = kOffMisc + 16;   // merges to do: [4 quadrants][count, b0, b1, -]
     static constexpr int kOffCum = kOffPend + 64;
     static constexpr int smem_bytes(int B) { return kOffCum + (B + 1) * 4 + 1024; }
     static_assert(kOffRecv % 1024 == 0 && kOffP % 1024 == 0 && kOffQR % 1024 == 0, "alignment");
-    static_assert(threads<F8>() * 4 <= kRecvBytes, "scan scratch lives in the exchange buffer");
-    static_assert(kF8RopeOff + 2048 == kStageBytes && kF8Bytes * 2 == kStageBytes, "E4M3 staging: half of every box");
+    static_assert(kThreads * 4 <= kRecvBytes, "scan scratch lives in the exchange buffer");
 };
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
@@ -111,65 +87,11 @@ constexpr uint32_t kTmemQ = 256;
 constexpr uint32_t kTmemS = 384;
 }  // namespace mla
 
-// E4M3 page -> f16 page, in place, by four warps.  The TMA left the codes of
-// c_kv box c (dims 64c .. 64c+63 of this CTA, [64 tokens][64]) at 8192 c +
-// 4096 and the k_R codes ([64][32]) at 34816.  Written: box c at 8192 c,
-// token t's row at 128 t, 16-byte chunk k (8 dims) at chunk k ^ (t & 7)
-// (128-byte swizzle); k_R at 32768, row t at 64 t, chunk k at
-// k ^ ((t >> 1) & 3) (64-byte swizzle) -- the layout the TMA gives a bf16
-// page.  Converter c widens box c (and converter 0 the rope box too): it
-// reads all of its codes into registers, then overwrites them, so no warp
-// touches another's bytes.  Lane work: item k (of 8) is 16 codes of token
-// 8k + (lane >> 2), dims 16 (lane & 3) .. + 15 of the box: a quarter-warp
-// reads 128 contiguous bytes and writes 8 distinct bank groups.
-namespace mla {
-KVDEC_DEVINL void widen_store2(uint8_t* p0, uint8_t* p1, uint4 x) {
-    uint32_t h[8];
-    e4m3x4_to_f16x2x2(x.x, h[0], h[1]);
-    e4m3x4_to_f16x2x2(x.y, h[2], h[3]);
-    e4m3x4_to_f16x2x2(x.z, h[4], h[5]);
-    e4m3x4_to_f16x2x2(x.w, h[6], h[7]);
-    *reinterpret_cast<uint4*>(p0) = make_uint4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<uint4*>(p1) = make_uint4(h[4], h[5], h[6], h[7]);
-}
-KVDEC_DEVINL void widen_box(uint8_t* st, int c, int lane) {
-    uint8_t* box = st + 8192 * c;
-    const int tl = lane >> 2, u = lane & 3;
-    uint4 x[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k)
-        x[k] = *reinterpret_cast<const uint4*>(box + kF8BoxOff + (8 * k + tl) * 64 + 16 * u);
-    uint4 xr[4];
-    const int tr = lane >> 1, v = lane & 1;   // rope: item k is token 16k + tr, codes 16 v .. + 15
-    if (c == 0) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) xr[k] = *reinterpret_cast<const uint4*>(st + kF8RopeOff + (16 * k + tr) * 32 + 16 * v);
-    }
-    __syncwarp();   // every lane has read its codes: they may be overwritten
-    // token 8k + tl: (8k + tl) & 7 = tl
-    const int c0 = ((2 * u) ^ tl) << 4, c1 = ((2 * u + 1) ^ tl) << 4;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        uint8_t* row = box + (8 * k + tl) * 128;
-        widen_store2(row + c0, row + c1, x[k]);
-    }
-    if (c == 0) {
-        // token 16k + tr: ((16k + tr) >> 1) & 3 = (tr >> 1) & 3
-        const int sw = (tr >> 1) & 3;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            uint8_t* row = st + 32768 + (16 * k + tr) * 64;
-            widen_store2(row + (((2 * v) ^ sw) << 4), row + (((2 * v + 1) ^ sw) << 4), xr[k]);
-        }
-    }
-}
-}  // namespace mla
-
-template <int NS, int PB, bool F8>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 1)
+template <int NS, int PB>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::kThreads, 1)
     mla_decode_kernel(const __grid_constant__ MlaMaps maps, const MlaArgs a) {
     using namespace mla;
-    using L = Layout<NS, PB, F8>;
+    using L = Layout<NS, PB>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -180,7 +102,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
     auto bar = [bar0](int i) { return bar0 + 8u * (uint32_t)i; };
     auto kv_full = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + s); };
     auto kv_empty = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + NS + s); };
-    auto codes_full = [bar0](int s) { return bar0 + 8u * (uint32_t)(B_KV + 2 * NS + s); };   // E4M3 only
     volatile int* misc = reinterpret_cast<volatile int*>(smem + L::kOffMisc);
     volatile int* abort_word = misc + 1;
     int* scratch = reinterpret_cast<int*>(smem + L::kOffRecv);   // free until the first exchange
@@ -204,9 +125,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
         for (int i = 0; i < 16; ++i) mbar_init(bar(B_HAND + i), 1);
         mbar_init(bar(B_DONE), 2);                  // both MMA issuers
         for (int s = 0; s < NS; ++s) {
-            mbar_init(kv_full(s), F8 ? kConvWarps : 1);   // E4M3: the converters' arrivals
+            mbar_init(kv_full(s), 1);
             mbar_init(kv_empty(s), 1);
-            if (F8) mbar_init(codes_full(s), 1);
         }
         misc[1] = 0;
         for (int q = 0; q < 4; ++q) pend[4 * q] = 0;
@@ -262,21 +182,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
                     report(a.err, KVDEC_DEVERR_BAD_PAGE);
                     page = 0;
                 }
+                const uint32_t fb = kv_full(stage);
                 const uint32_t dst = sKV + stage * kStageBytes;
-                if (F8) {
-                    const uint32_t fb = codes_full(stage);
-                    mbar_arrive_expect_tx(fb, kF8Bytes);
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_2d(dst + c * 8192 + kF8BoxOff, &maps.c128, fb, 256 * rank + 64 * c, page * kTileTokens,
-                                    pol);
-                    tma_load_2d(dst + kF8RopeOff, &maps.c64, fb, 512 + 32 * rank, page * kTileTokens, pol);
-                } else {
-                    const uint32_t fb = kv_full(stage);
-                    mbar_arrive_expect_tx(fb, kStageBytes);
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_2d(dst + c * 8192, &maps.c128, fb, 256 * rank + 64 * c, page * kTileTokens, pol);
-                    tma_load_2d(dst + 32768, &maps.c64, fb, 512 + 32 * rank, page * kTileTokens, pol);
-                }
+                mbar_arrive_expect_tx(fb, kStageBytes);
+                for (int c = 0; c < 4; ++c)
+                    tma_load_2d(dst + c * 8192, &maps.c128, fb, 256 * rank + 64 * c, page * kTileTokens, pol);
+                tma_load_2d(dst + 32768, &maps.c64, fb, 512 + 32 * rank, page * kTileTokens, pol);
                 ++issued;
                 if (++stage == NS) {
                     stage = 0;
@@ -288,8 +199,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
             }
             // never leave TMA writes in flight
             for (long long i = (issued > NS ? issued - NS : 0); i < issued; ++i)
-                if (!mbar_wait_bounded(F8 ? codes_full((int)(i % NS)) : kv_full((int)(i % NS)),
-                                       (uint32_t)((i / NS) & 1), a.timeout_ns)) {
+                if (!mbar_wait_bounded(kv_full((int)(i % NS)), (uint32_t)((i / NS) & 1), a.timeout_ns)) {
                     report(a.err, KVDEC_DEVERR_TIMEOUT);
                     break;
                 }
@@ -303,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
         // descriptors as a base plus constant offsets) and one elected lane
         // issues each MMA and commit; lane 0 parks in the slow waits.
         if (n > 0) {
-            constexpr uint32_t iS = F8 ? umma_idesc_f16(128, 64, false, false) : umma_idesc_bf16(128, 64, false, false);
+            constexpr uint32_t iS = umma_idesc_bf16(128, 64, false, false);
             const uint64_t dK = umma_desc(sKV, 16, 1024, kSwizzle128B);
             const uint64_t dKR = umma_desc(sKV + 32768, 16, 512, kSwizzle64B);
             const uint64_t dQR = umma_desc(sQR, 16, 512, kSwizzle64B);
@@ -345,7 +255,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
         // once the previous sequence's O has been flushed); then the page's
         // stage goes back to the producer.
         if (n > 0) {
-            constexpr uint32_t iP = F8 ? umma_idesc_f16(128, 256, false, true) : umma_idesc_bf16(128, 256, false, true);
+            constexpr uint32_t iP = umma_idesc_bf16(128, 256, false, true);
             const uint64_t dP = umma_desc(sP, 16, 1024, kSwizzle128B);
             const uint64_t dV = umma_desc(sKV, 8192, 1024, kSwizzle128B);
             auto wait1 = [&](uint32_t bb, uint32_t par) -> bool {
@@ -378,25 +288,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
             umma_commit_w(bar(B_DONE));
             if (lane == 0 && !mbar_wait_bounded(bar(B_DONE), 0, a.timeout_ns)) report(a.err, KVDEC_DEVERR_TIMEOUT);
         }
-    } else if (warp >= kSoftWarps + 3) {
-        // ------------------------------------------------------------ E4M3 converters
-        // page j's codes -> f16 in its stage, one box per warp; once all four
-        // have arrived the stage counts as loaded for the S issuer (kv_full);
-        // the stage itself is handed back by PV as for a bf16 page.
-        if (F8 && n > 0) {
-            const int cw = warp - (kSoftWarps + 3);
-            for (long long j = 0; j < n; ++j) {
-                const int stage = (int)(j % NS);
-                // every lane reads the codes, so every lane observes the phase
-                const bool ok = wait_or_abort(codes_full(stage), (uint32_t)((j / NS) & 1), abort_word, a.err,
-                                              a.timeout_ns);
-                if (!__all_sync(0xffffffffu, ok ? 1 : 0)) break;
-                widen_box(smem + L::kOffKV + stage * kStageBytes, cw, lane);
-                fence_proxy_async();   // the f16 page -> the tensor cores
-                __syncwarp();
-                if (lane == 0) mbar_arrive(kv_full(stage));
-            }
-        }
     } else {
         // ------------------------------------------------------------ softmax groups
         // Group g takes the pages j with j % 2 == g; thread (qd, lane) of a
@@ -412,10 +303,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
         const uint32_t peer_full = mapa_shared(bar(B_RECV_FULL), peer);
         const uint32_t peer_empty = mapa_shared(bar(B_RECV_EMPTY), peer);
         const float sl2 = a.scale_log2;
-        // E4M3 cache: Q_r goes to the tensor cores pre-multiplied by the
-        // scales, O takes the c_kv scale at the flush
-        const float sc_c = F8 ? __ldg(a.kv_scale) : 1.f;
-        const float sc_r = F8 ? __ldg(a.kv_scale + 1) : 1.f;
         uint32_t hand_waits[2] = {0u, 0u};
 
         // sequences with no tokens
@@ -435,9 +322,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
         // Q_r of sequence b, this group's half: latent dims [128 g, 128 g + 128)
         // -> TMEM (bf16 pairs), rope dims [16 g, 16 g + 16) -> shared memory,
         // K-major with the 64-byte swizzle (16-byte chunk c of row r stored at
-        // chunk c ^ ((r >> 1) & 3)).  E4M3 cache: f16 pairs of q_abs * sc_c and
-        // q_rope * sc_r.  Called once the previous sequence's last S has
-        // completed.
+        // chunk c ^ ((r >> 1) & 3)).  Called once the previous sequence's last
+        // S has completed.
         auto load_q = [&](int b) {
             const uint4* qa = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)b * kHeads + row) * 512 + 256 * rank + 128 * g);
             const uint4* qr = reinterpret_cast<const uint4*>(a.q_rope + ((size_t)b * kHeads + row) * 64 + 32 * rank);
@@ -445,13 +331,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
 #pragma unroll
             for (int i = 0; i < 16; ++i) x[i] = __ldg(qa + i);
 #pragma unroll
-            for (int c = 2 * g; c < 2 * g + 2; ++c) {
-                uint4 r4 = __ldg(qr + c);
-                if (F8)
-                    r4 = make_uint4(bf16x2_scaled_to_f16x2(r4.x, sc_r), bf16x2_scaled_to_f16x2(r4.y, sc_r),
-                                    bf16x2_scaled_to_f16x2(r4.z, sc_r), bf16x2_scaled_to_f16x2(r4.w, sc_r));
-                *reinterpret_cast<uint4*>(smem + L::kOffQR + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = r4;
-            }
+            for (int c = 2 * g; c < 2 * g + 2; ++c)
+                *reinterpret_cast<uint4*>(smem + L::kOffQR + row * 64 + ((c ^ ((row >> 1) & 3)) << 4)) = __ldg(qr + c);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t v[16];
@@ -461,10 +342,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
                     v[4 * k + 1] = x[4 * c + k].y;
                     v[4 * k + 2] = x[4 * c + k].z;
                     v[4 * k + 3] = x[4 * c + k].w;
-                }
-                if (F8) {
-#pragma unroll
-                    for (int k = 0; k < 16; ++k) v[k] = bf16x2_scaled_to_f16x2(v[k], sc_c);
                 }
                 tmem_st16u(trow + kTmemQ + 64 * g + 16 * c, v);
             }
@@ -618,20 +495,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
                 __syncwarp();
                 if (lane == 0) mbar_arrive(hbar);
             }
-            // ---- probabilities (base 2) -> registers, packed to bf16 pairs
-            // (E4M3 cache: f16 pairs of 2^7 p); they are computed before the
-            // wait for the P buffer, so only the stores below wait for PV(j-1)
+            // ---- probabilities (base 2) -> registers, packed to bf16 pairs; they
+            // are computed before the wait for the P buffer, so only the
+            // stores below wait for PV(j-1)
             uint32_t pk[32];
             float lsum;
             {
                 float ls[4] = {0.f, 0.f, 0.f, 0.f};
-                const float pb = F8 ? kPShift - m_new : -m_new;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = fast_exp2(fmaf(s[2 * i], sl2, pb));
-                    const float p1 = fast_exp2(fmaf(s[2 * i + 1], sl2, pb));
+                    const float p0 = fast_exp2(fmaf(s[2 * i], sl2, -m_new));
+                    const float p1 = fast_exp2(fmaf(s[2 * i + 1], sl2, -m_new));
                     ls[i & 3] += p0 + p1;
-                    pk[i] = F8 ? pack_half2(p0, p1) : pack_bf16x2(p0, p1);
+                    pk[i] = pack_bf16x2(p0, p1);
                 }
                 lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
             }
@@ -705,10 +581,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(mla::threads<F8>(), 
                 tc_fence_after();
                 const bool complete = (seg_start > 0 || lt0 == 0) && (cur.lt == cur.nt - 1);
                 const int slot = 2 * w + (seg_start == 0 ? 0 : 1);
-                // (E4M3: l_tot and O both carry the 2^7 of P; O takes the c_kv scale)
-                const float inv = l_tot > 0.f ? sc_c / l_tot : 0.f;
-                const float lse_v =
-                    l_tot > 0.f ? (m_new - (F8 ? kPShift : 0.f) + __log2f(l_tot)) * kLn2 : -INFINITY;
+                const float inv = l_tot > 0.f ? 1.f / l_tot : 0.f;
+                const float lse_v = l_tot > 0.f ? (m_new + __log2f(l_tot)) * kLn2 : -INFINITY;
                 const size_t orow = (size_t)cur.b * kHeads + row;
                 const int col0 = 256 * (int)rank;
                 // O / l goes out 32 columns at a time through this warp's quarter
@@ -936,40 +810,34 @@ int optin_smem() {
 // long-context run with them faulted the GPU; the cause is not found, so
 // that configuration is not built.
 static_assert(KVDEC_MLA_PB == 1, "the two-P-buffer configuration is not built");
+using Built = mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB>;
 // The per-sequence tile table shares the CTA's shared memory with the cache
 // stages, so the batch is bounded by what is left of the 227 KB a CTA of
-// sm_100 / sm_103 may opt in to; one bound serves both cache formats (the
-// E4M3 layout holds NS more barriers).  No other stage count is built.
-using BuiltF8 = mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB, true>;
-static_assert(BuiltF8::smem_bytes(0) >= mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB, false>::smem_bytes(0),
-              "the E4M3 layout is the larger");
+// sm_100 / sm_103 may opt in to.  No other stage count is built.
 constexpr int kOptinSmem = 227 * 1024;
-constexpr int kMaxBatch = (kOptinSmem - BuiltF8::smem_bytes(0)) / 4;
+constexpr int kMaxBatch = (kOptinSmem - Built::smem_bytes(0)) / 4;
 static_assert(kMaxBatch >= 256, "the five-stage layout leaves room for at least 256 sequences");
-template <bool F8>
-bool fits(int B) {
-    return B <= kMaxBatch && mla::Layout<KVDEC_MLA_NS, KVDEC_MLA_PB, F8>::smem_bytes(B) <= optin_smem();
-}
+bool fits(int B) { return B <= kMaxBatch && Built::smem_bytes(B) <= optin_smem(); }
 
-template <int NS, int PB, bool F8>
+template <int NS, int PB>
 cudaError_t launch_ns(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    const int smem = mla::Layout<NS, PB, F8>::smem_bytes(a.B);
-    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB, F8>));
+    const int smem = mla::Layout<NS, PB>::smem_bytes(a.B);
+    cudaError_t e = allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB>));
     if (e != cudaSuccess) return e;
-    mla_decode_kernel<NS, PB, F8><<<2 * pairs, mla::threads<F8>(), smem, st>>>(maps, a);
+    mla_decode_kernel<NS, PB><<<2 * pairs, mla::kThreads, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
-template <int NS, int PB, bool F8>
+template <int NS, int PB>
 int max_pairs_ns(int B) {
-    const int smem = mla::Layout<NS, PB, F8>::smem_bytes(B);
-    if (allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB, F8>)) != cudaSuccess) return 0;
+    const int smem = mla::Layout<NS, PB>::smem_bytes(B);
+    if (allow_max_dynamic_smem(reinterpret_cast<const void*>(mla_decode_kernel<NS, PB>)) != cudaSuccess) return 0;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(mla::threads<F8>(), 1, 1);
+    cfg.blockDim = dim3(mla::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -979,24 +847,17 @@ int max_pairs_ns(int B) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<NS, PB, F8>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<NS, PB>, &cfg) != cudaSuccess) return 0;
     return n;
 }
 }  // namespace
 
 cudaError_t launch_mla(const MlaMaps& maps, const MlaArgs& a, int pairs, cudaStream_t st) {
-    if (a.fp8) {
-        if (!fits<true>(a.B)) return cudaErrorInvalidValue;   // the host checks kMaxBatch first
-        return launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB, true>(maps, a, pairs, st);
-    }
-    if (!fits<false>(a.B)) return cudaErrorInvalidValue;
-    return launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB, false>(maps, a, pairs, st);
+    if (!fits(a.B)) return cudaErrorInvalidValue;   // the host checks kMaxBatch first
+    return launch_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(maps, a, pairs, st);
 }
 
-int max_pairs_mla(int B, bool fp8) {
-    if (fp8) return fits<true>(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB, true>(B) : 0;
-    return fits<false>(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB, false>(B) : 0;
-}
+int max_pairs_mla(int B) { return fits(B) ? max_pairs_ns<KVDEC_MLA_NS, KVDEC_MLA_PB>(B) : 0; }
 
 int max_batch_mla() { return kMaxBatch; }
 

@@ -199,14 +199,19 @@ kvdec_status kvdec_gqa_decode_noalloc(const kvdec_gqa_params* p, void* stream);
  * FP8 latent cache (kv_format = KVDEC_KV_FP8_E4M3): cache holds uint8 E4M3
  *   codes [num_pages, 64, 576] (576 bytes a token); kv_scale is a device
  *   array fp32 [2] (required): c_kv = E4M3(code[0:512]) * kv_scale[0],
- *   k_R = E4M3(code[512:576]) * kv_scale[1].  The tensor cores take f16
- *   operands on this path: q_absorbed * kv_scale[0] and q_rope * kv_scale[1]
- *   are rounded to f16 (magnitudes must stay below 65504).
+ *   k_R = E4M3(code[512:576]) * kv_scale[1].  The call first widens the
+ *   pages it reads into a bf16 copy in the workspace (each value
+ *   E4M3(code) * scale rounded once to bf16, nearest-even), then runs the
+ *   bf16 decode on the copy: the FP8 cache halves the bytes held in HBM,
+ *   not the bytes a step moves.  The workspace grows by
+ *   batch * max_blocks * (73728 + 4) bytes; batch * max_blocks * 64 must stay
+ *   below 2^31.
  * Supported: num_heads == 128 (tensor-core tile height) and
  * batch <= kvdec_mla_max_batch(): the kernel keeps a per-sequence tile table
  * in shared memory beside its cache stages, so a larger batch is rejected
  * with KVDEC_ERR_INVALID_ARG before any launch (split it into calls).
- * Workspace: as for kvdec_gqa_decode (no initialisation needed).
+ * Workspace: as for kvdec_gqa_decode (no initialisation needed), plus the
+ * widened copy for an FP8 cache.
  */
 typedef struct kvdec_mla_params {
     const void* q_absorbed;

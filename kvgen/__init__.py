@@ -210,15 +210,12 @@ def fp8_codes(x: torch.Tensor, g, device):
 
 
 def mla_fp8_codes(cache: torch.Tensor, g, device):
-    """Stand-in for a quantised E4M3 latent cache: the drawn N(0,1) c_kv
-    values times a spread sigma_c and the k_R values times sigma_R, both
-    ~ U[0.25, 4] (so that the two scales differ and a swap is visible),
-    cast by torch to float8_e4m3fn with scale = max|x| / 448 per piece.
-    Returns (uint8 codes of the cache's shape, fp32 [scale_c, scale_R])."""
-    sigma = torch.empty(2, device=device).uniform_(0.25, 4.0, generator=g)
+    """Stand-in for a quantised E4M3 latent cache: the drawn N(0,1) values
+    of the row (the same distribution as the bf16 cache), cast by torch to
+    float8_e4m3fn with one scale per piece, max|x| / 448 over the c_kv values
+    and over the k_R values.  Returns (uint8 codes of the cache's shape,
+    fp32 [scale_c, scale_R]).  ``g`` is unused (kept for a uniform call)."""
     x = cache.float()
-    x[..., :D_C] *= sigma[0]
-    x[..., D_C:] *= sigma[1]
     amax = torch.stack([x[..., :D_C].abs().amax(), x[..., D_C:].abs().amax()]).clamp(min=1e-6)
     scale = (amax / 448.0).to(torch.float32)
     x[..., :D_C] /= scale[0]

@@ -145,13 +145,11 @@ def test_prefill_argument_checks(lib):
 def test_mla_batch_limit(lib):
     """The MLA decode keeps a tile table of batch + 1 ints in shared memory
     beside five 36 KB cache stages, the 16 KB exchange and P buffers, the
-    8 KB rope part of Q, a 4 KB hand-off and the barriers (of the E4M3
-    layout, which has five more: one bound serves both cache formats); the
-    largest batch that fits in the 227 KB a CTA may use is the limit (403),
-    and one more sequence is rejected on the host (INVALID_ARG) before any
-    device query."""
+    8 KB rope part of Q and a 4 KB hand-off; the largest batch that fits in
+    the 227 KB a CTA may use is the limit (411), and one more sequence is
+    rejected on the host (INVALID_ARG) before any device query."""
     limit = lib.kvdec_mla_max_batch()
-    assert limit == 403
+    assert limit == 411
     m = kvdec.MlaParams()
     m.num_heads, m.num_pages, m.max_blocks = 128, 4, 4
     m.batch = limit + 1

@@ -100,6 +100,10 @@ __device__ __noinline__ void gqa_merge_unit(uint8_t* smem, TileSchedule S, int u
     };
     __threadfence();
     issue(0);   // the first round's pieces travel while the maxima are taken
+    // all pieces in one round (the usual case): each row's lse values are
+    // read once, kept in the weight buffer and turned into weights there by
+    // the same thread
+    const bool one_round = np <= per_round;
     if (tid < nr) {
         // max and denominator, four pieces' lse loads in flight
         float M = -INFINITY, den = 0.f;
@@ -108,6 +112,11 @@ __device__ __noinline__ void gqa_merge_unit(uint8_t* smem, TileSchedule S, int u
 #pragma unroll
             for (int u = 0; u < 4; ++u)
                 ls[u] = s2 + u < np ? __ldcg(part_lse + (size_t)slot_of(s2 + u) * hc_rows + tid) : -INFINITY;
+            if (one_round) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    if (s2 + u < np) wgt[(s2 + u) * ROWS + tid] = ls[u];
+            }
             const float Mn = fmaxf(fmaxf(M, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
             if (Mn != -INFINITY) {
                 den = (M == -INFINITY) ? 0.f : den * fast_exp2((M - Mn) * kLog2e);
@@ -119,6 +128,12 @@ __device__ __noinline__ void gqa_merge_unit(uint8_t* smem, TileSchedule S, int u
         rowml[tid * 2] = M;
         rowml[tid * 2 + 1] = den;
         if (lse_out) lse_out[(size_t)b * H + h0 + tid] = (den > 0.f) ? M + __logf(den) : -INFINITY;
+        if (one_round) {
+            for (int k = 0; k < np; ++k) {
+                const float ls = wgt[k * ROWS + tid];
+                wgt[k * ROWS + tid] = (ls == -INFINITY || !(den > 0.f)) ? 0.f : fast_exp2((ls - M) * kLog2e) / den;
+            }
+        }
     }
     named_barrier(1, 128);
     float4 acc[kElems];
@@ -127,7 +142,7 @@ __device__ __noinline__ void gqa_merge_unit(uint8_t* smem, TileSchedule S, int u
     for (int s0 = 0; s0 < np; s0 += per_round) {
         const int cnt = min(per_round, np - s0);
         if (s0 > 0) issue(s0);
-        for (int i = tid; i < cnt * nr; i += 128) {
+        for (int i = one_round ? cnt * nr : tid; i < cnt * nr; i += 128) {   // one round: weights already there
             const int k = i / nr, r = i % nr;
             const float ls = __ldcg(part_lse + (size_t)slot_of(s0 + k) * hc_rows + r);
             const float M = rowml[r * 2], den = rowml[r * 2 + 1];
@@ -616,14 +631,22 @@ __global__ void __launch_bounds__(160, 2)
         // then count them; keep the units whose count this completes
         __threadfence();
         named_barrier(1, 128);
-        if (tid == 0) {
-            int keep = 0;
-            for (int e = 0; e < misc[2]; ++e) {
-                const int unit = misc[3 + e];
+        if (warp == 0) {
+            // one lane per unit (at most two), both counts in flight together
+            const int np2 = misc[2];
+            bool last = false;
+            if (lane < np2) {
+                const int unit = misc[3 + lane];
                 const int b = unit / S.upb, jj = unit % S.upb;
-                if (arrive_piece(a.counters + unit, a.epoch, (uint32_t)S.num_pieces(b, jj))) misc[3 + keep++] = unit;
+                last = arrive_piece(a.counters + unit, a.epoch, (uint32_t)S.num_pieces(b, jj));
             }
-            misc[2] = keep;
+            const unsigned done = __ballot_sync(0xffffffffu, last);
+            if (lane == 0) {
+                int keep = 0;
+                for (int e = 0; e < np2; ++e)
+                    if ((done >> e) & 1u) misc[3 + keep++] = misc[3 + e];
+                misc[2] = keep;
+            }
         }
         named_barrier(1, 128);
     }

@@ -54,135 +54,11 @@ struct GqaSmem {
     static constexpr int kStat = kObuf + kRows * kOStride * 4;  // [4 warps][16][2]
     static constexpr int kRowML = kStat + 4 * 16 * 2 * 4;       // [rows][2]
     static constexpr int kBars = kRowML + kRows * 2 * 4;
-    static constexpr int kMisc = kBars + 2 * NS * 8;            // ints: abort, -, #pending, pending[2]
-    static constexpr int kScratch = kMisc + 8 * 4;
+    static constexpr int kMisc = kBars + 2 * NS * 8;            // ints
+    static constexpr int kScratch = kMisc + 4 * 4;
     static constexpr int kCum = kScratch + 160 * 4;
     static constexpr int bytes(int B) { return kCum + (B + 1) * 4 + 1024; }
 };
-
-// Merge of one split unit (b, KV head, head chunk) by the CTA that wrote its
-// last piece, after the CTA's tiles: the pieces are staged into the tile
-// ring with 16-byte asynchronous copies, as many per round as fit, so that a
-// round's loads are all in flight together; each thread then accumulates its
-// float4 elements from shared memory.  Kept out of line so that the tile
-// loop's registers do not depend on it.
-template <int D, int MT, int NS, bool F8>
-__device__ __noinline__ void gqa_merge_unit(uint8_t* smem, TileSchedule S, int unit, const float* part_o,
-                                            const float* part_lse, unsigned long long* counters, float* lse_out,
-                                            void* out, int out_bf16, int H, int g, int n_hc, int hc_rows) {
-    using L = GqaSmem<D, MT, NS, F8>;
-    constexpr int ROWS = L::kRows;
-    constexpr int kElems = (ROWS * (D / 4) + 127) / 128;   // float4 per thread
-    const int tid = threadIdx.x;
-    float* rowml = reinterpret_cast<float*>(smem + L::kRowML);
-    float* wgt = reinterpret_cast<float*>(smem + L::kObuf);   // [per round][ROWS] weights
-    const uint32_t ring = smem_addr(smem);
-    const float4* ring4 = reinterpret_cast<const float4*>(smem);
-    const int b = unit / S.upb, jj = unit % S.upb;
-    const int kvh = jj / n_hc, hc = jj % n_hc;
-    const int nr = min(hc_rows, g - hc * hc_rows);
-    const int h0 = kvh * g + hc * hc_rows;
-    const int np = S.num_pieces(b, jj);
-    int w0, kind0;
-    S.first_piece(b, jj, w0, kind0);
-    auto slot_of = [&](int sp) { return 2 * (w0 + sp) + (sp == 0 ? kind0 : 0); };
-    const int piece_f4 = nr * (D / 4);                       // float4 of one piece
-    // as many pieces as the ring holds, and no more weights than the output
-    // staging buffer holds ([per round][ROWS] <= ROWS x kOStride)
-    const int per_round = max(1, min((NS * L::kStageBytes) / (piece_f4 * 16), L::kOStride));
-    auto issue = [&](int s0) {
-        const int cnt = min(per_round, np - s0);
-        for (int k = 0; k < cnt; ++k) {
-            const float4* src = reinterpret_cast<const float4*>(part_o + (size_t)slot_of(s0 + k) * hc_rows * D);
-            for (int c = tid; c < piece_f4; c += 128) cp_async16(ring + (uint32_t)((k * piece_f4 + c) * 16), src + c);
-        }
-        cp_async_commit();
-    };
-    __threadfence();
-    issue(0);   // the first round's pieces travel while the maxima are taken
-    // all pieces in one round (the usual case): each row's lse values are
-    // read once, kept in the weight buffer and turned into weights there by
-    // the same thread
-    const bool one_round = np <= per_round;
-    if (tid < nr) {
-        // max and denominator, four pieces' lse loads in flight
-        float M = -INFINITY, den = 0.f;
-        for (int s2 = 0; s2 < np; s2 += 4) {
-            float ls[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                ls[u] = s2 + u < np ? __ldcg(part_lse + (size_t)slot_of(s2 + u) * hc_rows + tid) : -INFINITY;
-            if (one_round) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    if (s2 + u < np) wgt[(s2 + u) * ROWS + tid] = ls[u];
-            }
-            const float Mn = fmaxf(fmaxf(M, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
-            if (Mn != -INFINITY) {
-                den = (M == -INFINITY) ? 0.f : den * fast_exp2((M - Mn) * kLog2e);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) den += (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - Mn) * kLog2e);
-                M = Mn;
-            }
-        }
-        rowml[tid * 2] = M;
-        rowml[tid * 2 + 1] = den;
-        if (lse_out) lse_out[(size_t)b * H + h0 + tid] = (den > 0.f) ? M + __logf(den) : -INFINITY;
-        if (one_round) {
-            for (int k = 0; k < np; ++k) {
-                const float ls = wgt[k * ROWS + tid];
-                wgt[k * ROWS + tid] = (ls == -INFINITY || !(den > 0.f)) ? 0.f : fast_exp2((ls - M) * kLog2e) / den;
-            }
-        }
-    }
-    named_barrier(1, 128);
-    float4 acc[kElems];
-#pragma unroll
-    for (int m = 0; m < kElems; ++m) acc[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < np; s0 += per_round) {
-        const int cnt = min(per_round, np - s0);
-        if (s0 > 0) issue(s0);
-        for (int i = one_round ? cnt * nr : tid; i < cnt * nr; i += 128) {   // one round: weights already there
-            const int k = i / nr, r = i % nr;
-            const float ls = __ldcg(part_lse + (size_t)slot_of(s0 + k) * hc_rows + r);
-            const float M = rowml[r * 2], den = rowml[r * 2 + 1];
-            wgt[k * ROWS + r] = (ls == -INFINITY || !(den > 0.f)) ? 0.f : fast_exp2((ls - M) * kLog2e) / den;
-        }
-        cp_async_wait_all();
-        named_barrier(1, 128);
-#pragma unroll
-        for (int m = 0; m < kElems; ++m) {
-            const int i = tid + 128 * m;
-            if (i < piece_f4) {
-                const int r = i / (D / 4);
-                for (int k = 0; k < cnt; ++k) {
-                    const float wk = wgt[k * ROWS + r];
-                    const float4 v = ring4[k * piece_f4 + i];
-                    acc[m].x = fmaf(wk, v.x, acc[m].x);
-                    acc[m].y = fmaf(wk, v.y, acc[m].y);
-                    acc[m].z = fmaf(wk, v.z, acc[m].z);
-                    acc[m].w = fmaf(wk, v.w, acc[m].w);
-                }
-            }
-        }
-        named_barrier(1, 128);   // the next round refills the ring and the weights
-    }
-#pragma unroll
-    for (int m = 0; m < kElems; ++m) {
-        const int i = tid + 128 * m;
-        if (i < piece_f4) {
-            const int r = i / (D / 4), c4 = i % (D / 4);
-            const size_t off = ((size_t)b * H + h0 + r) * D + c4 * 4;
-            if (out_bf16) {
-                uint2 pk = make_uint2(pack_bf16x2(acc[m].x, acc[m].y), pack_bf16x2(acc[m].z, acc[m].w));
-                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + off) = pk;
-            } else {
-                *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + off) = acc[m];
-            }
-        }
-    }
-    if (tid == 0) counters[unit] = 0ull;
-}
 
 template <int D, int MT, int NS, bool F8>
 __global__ void __launch_bounds__(160, 2)
@@ -211,7 +87,6 @@ __global__ void __launch_bounds__(160, 2)
         }
         misc[0] = 0;
         misc[1] = 0;
-        misc[2] = 0;
         fence_barrier_init();
     }
     build_cum(cum, scratch, a.seqlens, a.B, a.cap, a.err, a.window);
@@ -538,7 +413,6 @@ __global__ void __launch_bounds__(160, 2)
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const int row = 16 * mt_w + quad + 8 * r;
-                        if (row >= nrows) continue;   // padding rows of the head chunk are never written out
                         const float M = rowml[row * 2];
                         float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
                         if constexpr (F8) {
@@ -605,55 +479,90 @@ __global__ void __launch_bounds__(160, 2)
                     a.part_lse[(size_t)slot * a.hc_rows + tid] = lse_v;
                 }
             }
-            // a piece of a cut unit is counted after this CTA's tiles (one
-            // fence for all its pieces, out of the tile loop), and the piece
-            // that completes the count merges the unit there too, when the
-            // tile ring is free to stage the pieces (only an item's first and
-            // last units can be cut: at most two)
-            if (!complete && tid == 0 && misc[2] < 2) {
-                misc[3 + misc[2]] = unit;
-                misc[2] = misc[2] + 1;
+            if (!complete) {
+                __threadfence();
+                named_barrier(1, 128);
+                if (tid == 0)
+                    misc[1] = arrive_piece(a.counters + unit, a.epoch,
+                                           (uint32_t)S.num_pieces(cur.b, cur.j)) ? 1 : 0;
+                named_barrier(1, 128);
+                if (misc[1]) {
+                    // last piece of this unit: merge every piece's partial.
+                    // Piece s lives in slot 2 (w0 + s) (+ kind0 for s = 0).
+                    __threadfence();
+                    const int np = S.num_pieces(cur.b, cur.j);
+                    int w0, kind0;
+                    S.first_piece(cur.b, cur.j, w0, kind0);
+                    if (tid < nrows) {
+                        // max and denominator in one pass, four pieces' loads in flight
+                        float M = -INFINITY, den = 0.f;
+                        for (int s2 = 0; s2 < np; s2 += 4) {
+                            float ls[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int sp = s2 + u;
+                                const int sl = 2 * (w0 + sp) + (sp == 0 ? kind0 : 0);
+                                ls[u] = sp < np ? __ldcg(a.part_lse + (size_t)sl * a.hc_rows + tid) : -INFINITY;
+                            }
+                            const float Mn = fmaxf(fmaxf(M, fmaxf(ls[0], ls[1])), fmaxf(ls[2], ls[3]));
+                            if (Mn != -INFINITY) {
+                                den = (M == -INFINITY) ? 0.f : den * fast_exp2((M - Mn) * kLog2e);
+#pragma unroll
+                                for (int u = 0; u < 4; ++u)
+                                    den += (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - Mn) * kLog2e);
+                                M = Mn;
+                            }
+                        }
+                        rowml[tid * 2] = M;
+                        rowml[tid * 2 + 1] = den;
+                        if (a.lse)
+                            a.lse[(size_t)cur.b * a.H + h0 + tid] = (den > 0.f) ? M + __logf(den) : -INFINITY;
+                    }
+                    named_barrier(1, 128);
+                    for (int i = tid; i < nrows * (D / 4); i += 128) {
+                        const int r = i / (D / 4), c4 = i % (D / 4);
+                        const float M = rowml[r * 2], den = rowml[r * 2 + 1];
+                        const float inv = den > 0.f ? 1.f / den : 0.f;
+                        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                        // four pieces' loads in flight per round trip
+                        for (int s2 = 0; s2 < np; s2 += 4) {
+                            float ls[4];
+                            float4 v[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int sp = s2 + u;
+                                const int sl = 2 * (w0 + sp) + (sp == 0 ? kind0 : 0);
+                                const bool ok = sp < np;
+                                ls[u] = ok ? __ldcg(a.part_lse + (size_t)sl * a.hc_rows + r) : -INFINITY;
+                                v[u] = ok ? __ldcg(reinterpret_cast<const float4*>(
+                                               a.part_o + ((size_t)sl * a.hc_rows + r) * D + c4 * 4))
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const float wgt = (ls[u] == -INFINITY) ? 0.f : fast_exp2((ls[u] - M) * kLog2e) * inv;
+                                acc.x = fmaf(wgt, v[u].x, acc.x);
+                                acc.y = fmaf(wgt, v[u].y, acc.y);
+                                acc.z = fmaf(wgt, v[u].z, acc.z);
+                                acc.w = fmaf(wgt, v[u].w, acc.w);
+                            }
+                        }
+                        const size_t off = ((size_t)cur.b * a.H + h0 + r) * D + c4 * 4;
+                        if (a.out_bf16) {
+                            uint2 pk = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+                            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.out) + off) = pk;
+                        } else {
+                            *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + off) = acc;
+                        }
+                    }
+                    if (tid == 0) a.counters[unit] = 0ull;
+                }
             }
             named_barrier(1, 128);
             seg_start = true;
         }
         cur.advance(S);
     }
-
-    // ---------------------------------------------------------------- merges
-    // Units whose last piece this CTA wrote: merge every piece's partial by
-    // log-sum-exp ([ARG] §五.2) once this CTA's tiles are done, so that the
-    // tile ring is free to stage the pieces.
-    named_barrier(1, 128);
-    if (misc[0]) return;   // aborted: the ring may still receive stray loads
-    if (misc[2] > 0) {
-        // this CTA's pieces of cut units are all written: make them visible,
-        // then count them; keep the units whose count this completes
-        __threadfence();
-        named_barrier(1, 128);
-        if (warp == 0) {
-            // one lane per unit (at most two), both counts in flight together
-            const int np2 = misc[2];
-            bool last = false;
-            if (lane < np2) {
-                const int unit = misc[3 + lane];
-                const int b = unit / S.upb, jj = unit % S.upb;
-                last = arrive_piece(a.counters + unit, a.epoch, (uint32_t)S.num_pieces(b, jj));
-            }
-            const unsigned done = __ballot_sync(0xffffffffu, last);
-            if (lane == 0) {
-                int keep = 0;
-                for (int e = 0; e < np2; ++e)
-                    if ((done >> e) & 1u) misc[3 + keep++] = misc[3 + e];
-                misc[2] = keep;
-            }
-        }
-        named_barrier(1, 128);
-    }
-    const int npend = misc[2];
-    for (int e = 0; e < npend; ++e)
-        gqa_merge_unit<D, MT, NS, F8>(smem, S, misc[3 + e], a.part_o, a.part_lse, a.counters, a.lse, a.out,
-                                      a.out_bf16, a.H, a.g, a.n_hc, a.hc_rows);
 }
 
 // ---------------------------------------------------------------- launcher

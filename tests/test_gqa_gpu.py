@@ -177,3 +177,47 @@ def test_mqa_vs_mha_workload(cuda_lib):
     out2, _ = cuda_lib.gqa_decode(case.q, k_rep, v_rep, case.seqlens, scale=case.scale)
     torch.cuda.synchronize()
     assert_attn_close(out1, f64(out2), "C2 MQA vs MHA")
+
+
+@pytest.mark.parametrize("kv_dtype,max_ctas", [("bf16", 2), ("bf16", 0), ("fp8", 2), ("fp8", 0)])
+def test_lazy_rescale_heavy_tail(cuda_lib, kv_dtype, max_ctas):
+    """Keys that line up with the first query head of their group at a few
+    later positions, each stronger than the last: that head's running max
+    jumps by 10-14 (base 2) at tiles past the first, in the token slots of
+    every consumer warp, so each warp rescales O mid-sequence."""
+    B, h, n_kv, d = 2, 8, 2, 128
+    case = kvgen.gqa_case(B, h, n_kv, d, seqlens=[3000, 1100], seed=230, device="cuda")
+    g = h // n_kv
+    # positions in tiles 2, 9, 15, 30 of the first sequence (and the
+    # in-range ones of the second), one in each warp's 16-token slice
+    spikes = [(2 * 64 + 5, 1.0), (9 * 64 + 21, 2.0), (15 * 64 + 38, 3.0), (30 * 64 + 60, 4.0)]
+    for b in range(B):
+        for kv in range(n_kv):
+            q0 = case.q[b, kv * g].float()
+            for t, alpha in spikes:
+                if t < int(case.seqlens[b]):
+                    case.k[b, kv, t] = (alpha * q0).to(torch.bfloat16)
+    kw = {}
+    if kv_dtype == "fp8":
+        # one scale per KV head from the values' own maxima (spikes included),
+        # so the quantised spikes keep their size
+        def quant(x):
+            sc = (x.float().abs().amax(dim=(0, 2, 3)) / 448.0).clamp(min=1e-6)
+            codes = (x.float() / sc.view(1, -1, 1, 1)).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+            return codes.view(torch.uint8), sc.to(torch.float32)
+        case.k, case.k_scale = quant(case.k)
+        case.v, case.v_scale = quant(case.v)
+        kw = dict(k_scale=case.k_scale, v_scale=case.v_scale)
+        ref, lref = gqa_full_oracle(case)
+    else:
+        ref, lref = full_oracle(case)
+    # the jumps are there: the first head's base-2 score at each spike
+    # exceeds the running max before it by more than 8
+    sc = f64(case.q[0, 0:1]) @ (oracle.dequant_e4m3(case.k.cpu().numpy(), case.k_scale.cpu().numpy())[0, 0]
+                                if kv_dtype == "fp8" else f64(case.k[0, 0])).T
+    s2 = (sc[0, :3000] * case.scale / np.log(2))
+    jumps = [s2[t] - s2[:t].max() for t, _ in spikes[1:]]
+    assert min(jumps) > 8.0, jumps
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas, **kw)
+    assert_attn_close(out, ref, f"heavy tail {kv_dtype} max_ctas={max_ctas}")
+    assert_lse_close(lse, lref)

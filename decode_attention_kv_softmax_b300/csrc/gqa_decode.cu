@@ -60,6 +60,16 @@ struct GqaSmem {
     static constexpr int bytes(int B) { return kCum + (B + 1) * 4 + 1024; }
 };
 
+// 16-byte shared-memory load
+KVDEC_DEVINL uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 template <int D, int MT, int NS, bool F8>
 __global__ void __launch_bounds__(160, 2)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -325,15 +335,20 @@ __global__ void __launch_bounds__(160, 2)
                 const uint32_t keep_lo = (tk < n_valid ? 0x0000ffffu : 0u) | (tk + 1 < n_valid ? 0xffff0000u : 0u);
                 const uint32_t keep_hi = (tk + 8 < n_valid ? 0x0000ffffu : 0u) | (tk + 9 < n_valid ? 0xffff0000u : 0u);
                 if constexpr (F8) {
-                    // tokens tk, tk+1, tk+8, tk+9 (the B fragment's k rows);
-                    // per 32-dim block c a thread reads dims 32 c + 4 quad .. +3
+                    // tokens tk, tk+1, tk+8, tk+9 (the B fragment's k rows): a
+                    // thread takes dims 16 quad .. 16 quad + 15 of each, one
+                    // 16-byte load per token (a quarter-warp's loads hit eight
+                    // distinct bank groups under the swizzle); word c holds dims
+                    // 16 quad + 4 c .. +3
+                    const uint4 x0 = ld_shared_v4(vb + swz128(tk, quad));
+                    const uint4 x1 = ld_shared_v4(vb + swz128(tk + 1, quad));
+                    const uint4 x2 = ld_shared_v4(vb + swz128(tk + 8, quad));
+                    const uint4 x3 = ld_shared_v4(vb + swz128(tk + 9, quad));
+                    const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
+                    const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
                     for (int c = 0; c < D / 32; ++c) {
-                        const uint32_t chunk = 2 * c + (quad >> 2), sub = 4 * (quad & 3);
-                        const uint32_t w0 = ld_shared_u32(vb + swz128(tk, chunk) + sub);
-                        const uint32_t w1 = ld_shared_u32(vb + swz128(tk + 1, chunk) + sub);
-                        const uint32_t w2 = ld_shared_u32(vb + swz128(tk + 8, chunk) + sub);
-                        const uint32_t w3 = ld_shared_u32(vb + swz128(tk + 9, chunk) + sub);
+                        const uint32_t w0 = y0[c], w1 = y1[c], w2 = y2[c], w3 = y3[c];
                         // byte pairs per dim (dims 0, 1 | dims 2, 3), widened:
                         // bl[i] = tokens (tk, tk+1) of dim i, bh[i] = (tk+8, tk+9)
                         uint32_t bl[4], bh[4];
@@ -416,19 +431,19 @@ __global__ void __launch_bounds__(160, 2)
                         const float M = rowml[row * 2];
                         float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
                         if constexpr (F8) {
-                            // FP8: output tile nd = 4 c + i holds dims 32 c + 8 qc + i (+4)
+                            // FP8: output tile nd = 4 c + i holds dims 32 qc + 4 c + i (+16)
                             sc *= __ldg(a.v_scale + kvh);
-                            float* dst = obuf + row * L::kOStride + 8 * qc;
+                            float* dst = obuf + row * L::kOStride + 32 * qc;
 #pragma unroll
                             for (int nd = 0; nd < D / 8; ++nd) {
-                                float* p0 = dst + 32 * (nd >> 2) + (nd & 3);
+                                float* p0 = dst + 4 * (nd >> 2) + (nd & 3);
                                 const float v0 = o[nd][2 * r] * sc, v1 = o[nd][2 * r + 1] * sc;
                                 if (step == 0) {
                                     p0[0] = v0;
-                                    p0[4] = v1;
+                                    p0[16] = v1;
                                 } else {
                                     p0[0] += v0;
-                                    p0[4] += v1;
+                                    p0[16] += v1;
                                 }
                             }
                             continue;

@@ -27,11 +27,11 @@
 //    on the 8-bit rows hands a thread 4 consecutive dims of one token, so
 //    the contraction order inside each 16-dim step is permuted (thread t
 //    holds dims 4t..4t+3) and the Q fragments are loaded in that order.  V:
-//    each thread reads one 32-bit word (4 dims) from each of its 4 tokens,
-//    and a byte permute pairs the tokens per dim, giving the B fragment of
-//    dim 4g+i for output tile i; the output columns are mapped back at the
-//    flush.  The K scale folds into the softmax scale, the V scale into the
-//    final normalisation.
+//    each thread reads its 16 dims of each of its 4 tokens with one 16-byte
+//    load per token, and byte permutes pair the tokens per dim, giving the
+//    B fragment of dim 16g + 4c + i for output tile 4c + i; the output
+//    columns are mapped back at the flush.  The K scale folds into the
+//    softmax scale, the V scale into the final normalisation.
 //  * Sliding window ([ARG] §五.3): with a ring cache of w slots a step reads
 //    the min(seqlen, w) slots holding the last w tokens (read_len).
 #include "common.cuh"

@@ -13,13 +13,21 @@
 //
 // One CTA per (sequence, tile) slot; slots past the sequence's page count
 // only write their identity entry.  An HBM stream: 576 bytes read and 1152
-// written per token, coalesced 16-byte accesses.
+// written per token, coalesced 16-byte loads and 32-byte stores (the copy's
+// pages start on 32-byte boundaries: the workspace is 256-byte aligned and a
+// page is 73,728 bytes).
 #include "common.cuh"
 #include "kernels.h"
 
 namespace kvdec {
 
 namespace {
+// 32-byte global store (one instruction for 16 widened values; 32-byte aligned)
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+                 "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
 constexpr int kRow = KVDEC_MLA_DC + KVDEC_MLA_DR;        // 576 values a token
 constexpr int kPageVals = KVDEC_PAGE_SIZE * kRow;         // 36864
 constexpr int kChunks = kPageVals / 16;                   // 16 codes per chunk
@@ -60,8 +68,7 @@ __global__ void __launch_bounds__(kThreads) mla_widen_kernel(const MlaWidenArgs 
             o[2 * q] = pack_bf16x2(f0.x * s, f0.y * s);
             o[2 * q + 1] = pack_bf16x2(f1.x * s, f1.y * s);
         }
-        dst[2 * c] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[2 * c + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+        st_global_v8(dst + 2 * c, o);
     }
 }
 

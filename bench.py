@@ -711,18 +711,28 @@ def bench_combine(args):
     time.sleep(0.3)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    spin_end = torch.cuda.Event()
     # a single ~55 us kernel per step is shorter than the host's enqueue of
     # a step: hold the stream with a spin kernel (before the timed region)
     # while all steps are enqueued, so the launches run back to back and the
-    # per-launch events time the kernel, not host gaps
-    torch.cuda._sleep(int(args.steps * 4e5))
-    t0.record(stream)
-    for i in range(args.steps):
-        evs[i][0].record(stream)
-        step(i)
-        evs[i][1].record(stream)
-    t1.record(stream)
-    torch.cuda.synchronize()
+    # per-launch events time the kernel, not host gaps.  If the spin has
+    # already ended when the last step is enqueued (a slow host), the
+    # launches may have waited for it: time again with a longer spin.
+    spin = int(args.steps * 4e5)
+    for _attempt in range(4):
+        torch.cuda._sleep(spin)
+        spin_end.record(stream)
+        t0.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step(i)
+            evs[i][1].record(stream)
+        t1.record(stream)
+        overran = spin_end.query()
+        torch.cuda.synchronize()
+        if not overran:
+            break
+        spin *= 4
     clocks = clk.stop()
     ms = t0.elapsed_time(t1) / args.steps
     per = [e[0].elapsed_time(e[1]) * 1e3 for e in evs]

@@ -57,3 +57,41 @@ def test_mla_decode_replays(cuda_lib):
         torch.cuda.synchronize()
         assert_attn_close(out, ref, f"replay {r}")
         assert_lse_close(lse, lref, f"replay {r}")
+
+
+def test_mla_fp8_decode_replays(cuda_lib):
+    """The E4M3 latent cache: the widening pass and the decode captured
+    together; between replays the cache's codes change, and every replay
+    widens the new codes (the copy is rewritten, not reused)."""
+    case = kvgen.mla_case(3, 128, seqlens=[2500, 640, 1800], seed=83, device="cuda", kv_dtype="fp8")
+    run = lambda: cuda_lib.mla_decode_absorbed(case.q_abs, case.q_rope, case.cache, case.block_table,
+                                               case.seqlens, scale=case.scale, max_ctas=10,
+                                               kv_scale=case.kv_scale)
+    g, (out, lse) = capture(run)
+    gen = torch.Generator(device="cuda").manual_seed(84)
+    for r in range(REPLAYS):
+        if r > 0:   # new codes in place (same tensor the graph reads)
+            x = torch.randn(case.cache.shape, generator=gen, device="cuda").to(torch.bfloat16)
+            case.cache.copy_(kvgen.mla_fp8_codes(x, gen, "cuda")[0])
+        ref, lref = mla_full_oracle(case)
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_attn_close(out, ref, f"replay {r}")
+        assert_lse_close(lse, lref, f"replay {r}")
+
+
+def test_gqa_fp8_window_replays(cuda_lib):
+    case = kvgen.gqa_case(2, 32, 8, 128, seqlens=[3000, 700], paged=True, seed=85, device="cuda",
+                          kv_dtype="fp8", window=512)
+    run = lambda: cuda_lib.gqa_decode(case.q, case.k, case.v, case.seqlens, case.block_table,
+                                      scale=case.scale, k_scale=case.k_scale, v_scale=case.v_scale,
+                                      window=case.window, max_ctas=24)
+    g, (out, lse) = capture(run)
+    ref, lref = gqa_full_oracle(case)
+    for r in range(REPLAYS):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_attn_close(out, ref, f"replay {r}")
+        assert_lse_close(lse, lref, f"replay {r}")

@@ -44,6 +44,25 @@ def test_matches_workspace_entry_point_on_two_calls(cuda_lib):
         assert_lse_close(lse, olse, f"call {i} vs oracle")
 
 
+@pytest.mark.parametrize("paged,window", [(False, 0), (True, 0), (True, 300)])
+def test_fp8_and_window_through_the_array(cuda_lib, paged, window):
+    """The E4M3 cache and the sliding-window ring through the same entry
+    point, against the oracle, with the split counters left in the array by
+    the calls before (an empty sequence and one cut across many CTAs)."""
+    case = kvgen.gqa_case(3, 32, 8, 128, seqlens=[0, 2600, 450], cap=2688, paged=paged,
+                          seed=73 + window, device="cuda", kv_dtype="fp8", window=window)
+    flag = cuda_lib.new_error_flag()
+    out, lse = cuda_lib.gqa_decode_noalloc(case.q, case.k, case.v, case.seqlens, case.block_table,
+                                           scale=case.scale, k_scale=case.k_scale, v_scale=case.v_scale,
+                                           window=case.window, error_flag=flag, max_ctas=40)
+    torch.cuda.synchronize()
+    assert flag.item() == 0
+    ref, lref = gqa_full_oracle(case)
+    assert_attn_close(out, ref, f"fp8 paged={paged} window={window}")
+    assert_lse_close(lse, lref)
+    assert torch.all(out[0] == 0) and torch.isneginf(lse[0]).all()
+
+
 def test_rejects_problems_beyond_the_array(cuda_lib):
     lib = kvdec.load()
     p = kvdec.GqaParams()

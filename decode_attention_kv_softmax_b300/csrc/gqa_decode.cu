@@ -256,7 +256,10 @@ __global__ void __launch_bounds__(160, 2)
                 const uint32_t tok = tok_base + nt * 8 + (lane & 7);
                 if constexpr (F8) {
                     // 8-bit rows of 128 dims: matrix i of the x4 load is the
-                    // 16-dim step 4 kk + i; a thread gets dims 4 qc .. 4 qc + 3
+                    // 16-dim step 4 kk + i; a thread gets dims 4 qc .. 4 qc + 3.
+                    // Odd steps accumulate apart, so two chains of four
+                    // dependent MMAs run side by side instead of one of eight.
+                    float s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int kk = 0; kk < D / 64; ++kk) {
                         const uint32_t chunk = 4 * kk + (lane >> 3);
@@ -266,9 +269,11 @@ __global__ void __launch_bounds__(160, 2)
                         for (int i = 0; i < 4; ++i) {
                             uint32_t b0, b1;
                             e4m3x4_to_f16x2x2(r[i], b0, b1);
-                            mma_f16_16816(s[nt], qa[4 * kk + i], b0, b1);
+                            mma_f16_16816((i & 1) ? s2 : s[nt], qa[4 * kk + i], b0, b1);
                         }
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
                 } else {
 #pragma unroll
                     for (int kk = 0; kk < D / 32; ++kk) {

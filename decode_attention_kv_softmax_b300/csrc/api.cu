@@ -210,7 +210,7 @@ kvdec_status encode_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t
 
 struct GqaPlan {
     int D, MT, g, n_hc, hc_rows, units;
-    bool f8;
+    bool f8, dense;
     int grid;
     size_t off_lse, off_o, bytes;
 };
@@ -243,14 +243,35 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     pl.g = p->num_heads / p->num_kv_heads;
     pl.hc_rows = pl.g <= 32 ? pl.g : 32;
     pl.n_hc = (pl.g + pl.hc_rows - 1) / pl.hc_rows;
-    pl.MT = pl.hc_rows > 16 ? 2 : 1;
+    // row tiles of 16 head rows; an FP8 cache with at most 8 rows per chunk
+    // takes the transposed form (the rows as the MMA's 8 columns)
+    pl.MT = pl.hc_rows > 16 ? 2 : (pl.f8 && pl.hc_rows <= 8) ? 0 : 1;
     pl.units = p->batch * p->num_kv_heads * pl.n_hc;
     DeviceInfo di;
     int dev;
     if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
-    const int occ = cached_occupancy(std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch),
-                                     [&] { return kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, p->batch); });
+    int occ = cached_occupancy(std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch),
+                               [&] { return kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, false, p->batch); });
     if (occ < 1) return fail(KVDEC_ERR_CUDA, "GQA kernel does not fit on this device");
+    // The transposed FP8 form runs three CTAs per SM when the cache holds at
+    // most 256 tiles per SM (short contexts: the kernel's start and tail weigh
+    // most there); longer caches stream better through two CTAs of six stages.
+    pl.dense = false;
+    if (pl.MT == 0) {
+        long long slots = p->block_table ? (long long)p->max_blocks * KVDEC_PAGE_SIZE : p->capacity;
+        if (p->window > 0 && p->window < slots) slots = p->window;
+        const long long max_tiles =
+            (long long)pl.units * ((std::max(slots, 0ll) + KVDEC_PAGE_SIZE - 1) / KVDEC_PAGE_SIZE);
+        if (max_tiles <= 256ll * di.sm_count) {
+            const int occ3 = cached_occupancy(std::make_tuple(dev, 3, pl.D, pl.MT, p->batch), [&] {
+                return kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, true, p->batch);
+            });
+            if (occ3 >= 3) {
+                pl.dense = true;
+                occ = occ3;
+            }
+        }
+    }
     pl.grid = di.sm_count * occ;
     // max_ctas > 0 sets the number of work items (CTAs); above one resident
     // wave the hardware hands the equal-size items out as SMs free up.
@@ -439,7 +460,8 @@ kvdec_status kvdec_gqa_decode(const kvdec_gqa_params* p, void* stream) {
     a.k_scale = p->k_scale;
     a.v_scale = p->v_scale;
     a.window = p->window;
-    cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, pl.f8, tk, tv, a, pl.grid, static_cast<cudaStream_t>(stream));
+    cudaError_t e = kvdec::launch_gqa(pl.D, pl.MT, pl.f8, pl.dense, tk, tv, a, pl.grid,
+                                      static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "GQA decode launch");
     return KVDEC_OK;
 }

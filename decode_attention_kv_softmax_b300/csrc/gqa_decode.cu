@@ -32,6 +32,16 @@
 //    B fragment of dim 16g + 4c + i for output tile 4c + i; the output
 //    columns are mapped back at the flush.  The K scale folds into the
 //    softmax scale, the V scale into the final normalisation.
+//  * FP8 with at most 8 query heads per KV head (MT = 0): the same step
+//    transposed, S^T = K Q^T and O^T = V^T P^T, so that the warp's 16 tokens
+//    and then 16-dim slices of the head fill the MMA's 16 rows and the heads
+//    its 8 columns.  Against 16 padded head rows this halves the MMAs, the
+//    rescaled accumulators and the Q registers per token; the K codes widen
+//    straight into A fragments, P^T reaches the B operand through an in-
+//    register 8x8 transpose (movmatrix), and a thread ends up holding 16
+//    consecutive dims of two heads.  Built with two CTAs per SM of six
+//    stages, and with three of four stages (128 registers) for caches of at
+//    most 256 tiles per SM.
 //  * Sliding window ([ARG] §五.3): with a ring cache of w slots a step reads
 //    the min(seqlen, w) slots holding the last w tokens (read_len).
 #include "common.cuh"
@@ -48,7 +58,7 @@ struct GqaSmem {
     static constexpr int kBoxes = D / kBoxElems;
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kRows = 16 * MT;
+    static constexpr int kRows = MT == 0 ? 8 : 16 * MT;        // head rows of a chunk
     static constexpr int kOStride = D + 8;                    // padded fp32 row
     static constexpr int kObuf = NS * kStageBytes;
     static constexpr int kStat = kObuf + kRows * kOStride * 4;  // [4 warps][16][2]
@@ -59,6 +69,15 @@ struct GqaSmem {
     static constexpr int kCum = kScratch + 160 * 4;
     static constexpr int bytes(int B) { return kCum + (B + 1) * 4 + 1024; }
 };
+
+// Transpose of an 8x8 matrix of 16-bit values spread over the warp as an
+// MMA fragment (thread t holds row t / 4, columns 2 (t % 4) and 2 (t % 4) + 1),
+// returned in the same layout.
+KVDEC_DEVINL uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
 
 // 16-byte shared-memory load
 KVDEC_DEVINL uint4 ld_shared_v4(uint32_t addr) {
@@ -71,10 +90,15 @@ KVDEC_DEVINL uint4 ld_shared_v4(uint32_t addr) {
 }
 
 template <int D, int MT, int NS, bool F8>
-__global__ void __launch_bounds__(160, 2)
+__global__ void __launch_bounds__(160, (MT == 0 && NS == 4) ? 3 : 2)
     gqa_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const GqaArgs a) {
     static_assert(!F8 || D == 128, "the FP8 path is built for head_dim 128");
+    // MT = 0: at most 8 head rows, computed transposed (S^T = K Q^T and
+    // O^T = V^T P^T: tokens and dims fill the MMA's 16 rows, the head rows
+    // its 8 columns)
+    constexpr bool SW = (MT == 0);
+    static_assert(!SW || F8, "the transposed form is built for the FP8 cache");
     using L = GqaSmem<D, MT, NS, F8>;
     constexpr int ROWS = L::kRows;
     extern __shared__ uint8_t smem_raw[];
@@ -168,8 +192,9 @@ __global__ void __launch_bounds__(160, 2)
     // ---------------------------------------------------------------- consumers
     // Warp roles: warp w owns M-tile mt_w (16 head rows) and TPW tokens of
     // every tile, so a warp's registers do not depend on the group size.
-    constexpr int WPM = 4 / MT;          // warps per M-tile
-    constexpr int TPW = 16 * MT;         // tokens per warp per tile
+    // Transposed (SW): every warp holds all 8 rows and 16 tokens of a tile.
+    constexpr int WPM = SW ? 4 : 4 / MT; // warps per M-tile
+    constexpr int TPW = SW ? 16 : 16 * MT;  // tokens per warp per tile
     constexpr int NT = TPW / 8;          // 8-token MMA column tiles per warp
     const int quad = lane >> 2, qc = lane & 3;
     const int mt_w = warp / WPM;
@@ -200,8 +225,10 @@ __global__ void __launch_bounds__(160, 2)
     int stage = 0;
     uint32_t phase = 0;
 
-    uint32_t qa[D / 16][4];
-    float o[D / 8][4];
+    // SW: qa[ks] = the B fragment of Q^T for 16-dim step ks; o[nd] = O^T for
+    // dims 16 quad + 2 nd, + 1 (rows 2 qc, 2 qc + 1)
+    uint32_t qa[D / 16][SW ? 2 : 4];
+    float o[SW ? D / 16 : D / 8][4];
     float m[2], l[2];
     int len = 0, nrows = 0;
     bool seg_start = true, seg_item_first = true, seg_unit_first = true;
@@ -217,177 +244,286 @@ __global__ void __launch_bounds__(160, 2)
             nrows = min(a.hc_rows, a.g - hc * a.hc_rows);
             const int h0 = kvh * a.g + hc * a.hc_rows;
             if (F8) sl2 = a.scale_log2 * __ldg(a.k_scale + kvh);
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const int r = 16 * mt_w + quad + 8 * half;
+            if constexpr (SW) {
+                // column quad of Q^T = head row quad; its k order within each
+                // 16-dim step follows the K fragments (dims 4 qc .. 4 qc + 3)
                 const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-                    a.q + ((size_t)cur.b * a.H + h0 + min(r, nrows - 1)) * D);
-                const bool ok = r < nrows;
+                    a.q + ((size_t)cur.b * a.H + h0 + min(quad, nrows - 1)) * D);
+                const bool ok = quad < nrows;
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks) {
-                    if (F8) {
-                        // dims 16 ks + 4 qc .. +3, in the order the K fragments use
-                        const uint2 u = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 8 + 2 * qc))
-                                           : make_uint2(0u, 0u);
-                        qa[ks][half] = bf16x2_to_f16x2(u.x);
-                        qa[ks][half + 2] = bf16x2_to_f16x2(u.y);
-                    } else {
-                        qa[ks][half] = ok ? __ldg(qrow + ks * 8 + qc) : 0u;
-                        qa[ks][half + 2] = ok ? __ldg(qrow + ks * 8 + 4 + qc) : 0u;
+                    const uint2 u = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 8 + 2 * qc))
+                                       : make_uint2(0u, 0u);
+                    qa[ks][0] = bf16x2_to_f16x2(u.x);
+                    qa[ks][1] = bf16x2_to_f16x2(u.y);
+                }
+            } else {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int r = 16 * mt_w + quad + 8 * half;
+                    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+                        a.q + ((size_t)cur.b * a.H + h0 + min(r, nrows - 1)) * D);
+                    const bool ok = r < nrows;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        if constexpr (F8) {
+                            // dims 16 ks + 4 qc .. +3, in the order the K fragments use
+                            const uint2 u = ok ? __ldg(reinterpret_cast<const uint2*>(qrow + ks * 8 + 2 * qc))
+                                               : make_uint2(0u, 0u);
+                            qa[ks][half] = bf16x2_to_f16x2(u.x);
+                            qa[ks][half + 2] = bf16x2_to_f16x2(u.y);
+                        } else {
+                            qa[ks][half] = ok ? __ldg(qrow + ks * 8 + qc) : 0u;
+                            qa[ks][half + 2] = ok ? __ldg(qrow + ks * 8 + 4 + qc) : 0u;
+                        }
                     }
                 }
             }
             m[0] = m[1] = -INFINITY;
             l[0] = l[1] = 0.f;
 #pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+            for (int nd = 0; nd < (SW ? D / 16 : D / 8); ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
         }
         const int n_valid = min(kTileTokens, len - cur.lt * kTileTokens);
 
         if (wait_or_abort(full0 + 8 * stage, phase, misc, a.err, a.timeout_ns)) {
             const uint32_t kb = smem_addr(smem + stage * L::kStageBytes);
             const uint32_t vb = kb + L::kTileBytes;
-            // ---- S = Q K^T over this warp's TPW tokens
-            float s[NT][4];
+            if constexpr (SW) {
+                // ---- S^T = K Q^T: rows = this warp's 16 tokens, columns = the
+                // 8 head rows.  An x4 ldmatrix on the 8-bit rows gives tokens
+                // 0-7 / 8-15 of two 16-dim steps; a thread gets 4 consecutive
+                // dims of one token, widened to the A fragment in the k order
+                // of the Q^T fragments.  Two chains of four MMAs.
+                float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t krow = tok_base + (lane & 7) + (lane & 8);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t tok = tok_base + nt * 8 + (lane & 7);
-                if constexpr (F8) {
-                    // 8-bit rows of 128 dims: matrix i of the x4 load is the
-                    // 16-dim step 4 kk + i; a thread gets dims 4 qc .. 4 qc + 3.
-                    // Odd steps accumulate apart, so two chains of four
-                    // dependent MMAs run side by side instead of one of eight.
-                    float s2[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int kk = 0; kk < D / 64; ++kk) {
-                        const uint32_t chunk = 4 * kk + (lane >> 3);
-                        uint32_t r[4];
-                        ldsm_x4(kb + swz128(tok, chunk), r[0], r[1], r[2], r[3]);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            uint32_t b0, b1;
-                            e4m3x4_to_f16x2x2(r[i], b0, b1);
-                            mma_f16_16816((i & 1) ? s2 : s[nt], qa[4 * kk + i], b0, b1);
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < D / 32; ++kk) {
-                        const uint32_t chunk = 4 * kk + (lane >> 3);
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4(kb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
-                        mma_bf16_16816(s[nt], qa[2 * kk], r0, r1);
-                        mma_bf16_16816(s[nt], qa[2 * kk + 1], r2, r3);
-                    }
+                for (int kk = 0; kk < D / 32; ++kk) {
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kb + swz128(krow, 2 * kk + (lane >> 4)), r0, r1, r2, r3);
+                    uint32_t ka[4], kc[4];
+                    e4m3x4_to_f16x2x2(r0, ka[0], ka[2]);
+                    e4m3x4_to_f16x2x2(r1, ka[1], ka[3]);
+                    e4m3x4_to_f16x2x2(r2, kc[0], kc[2]);
+                    e4m3x4_to_f16x2x2(r3, kc[1], kc[3]);
+                    mma_f16_16816(s, ka, qa[2 * kk][0], qa[2 * kk][1]);
+                    mma_f16_16816(s2, kc, qa[2 * kk + 1][0], qa[2 * kk + 1][1]);
                 }
-            }
-            const bool partial = n_valid < kTileTokens;
-            if (partial) {
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const int tk = tok_base + nt * 8 + 2 * qc;
-                    if (tk >= n_valid) s[nt][0] = s[nt][2] = -INFINITY;
-                    if (tk + 1 >= n_valid) s[nt][1] = s[nt][3] = -INFINITY;
+                for (int e = 0; e < 4; ++e) s[e] += s2[e];
+                // s[0], s[1]: token tok_base + quad, head rows 2 qc, 2 qc + 1;
+                // s[2], s[3]: token tok_base + quad + 8, the same rows
+                const bool partial = n_valid < kTileTokens;
+                if (partial) {
+                    if (tok_base + quad >= n_valid) s[0] = s[1] = -INFINITY;
+                    if (tok_base + quad + 8 >= n_valid) s[2] = s[3] = -INFINITY;
                 }
-            }
-            // ---- online softmax (base 2, scaled) and P fragments
-            float mx0 = -INFINITY, mx1 = -INFINITY;
+                // ---- online softmax down the columns (across the 8 quads)
+                float mx0 = fmaxf(s[0], s[2]), mx1 = fmaxf(s[1], s[3]);
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
-                mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
-            }
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-            const float mn0 = fmaxf(m[0], mx0 * sl2), mn1 = fmaxf(m[1], mx1 * sl2);
-            const float b0 = (mn0 == -INFINITY) ? 0.f : mn0;
-            const float b1 = (mn1 == -INFINITY) ? 0.f : mn1;
-            const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
-            m[0] = mn0;
-            m[1] = mn1;
-            float ps0 = 0.f, ps1 = 0.f;
-            uint32_t pa[MT][4];
+                for (int x = 4; x < 32; x <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+                }
+                const float mn0 = fmaxf(m[0], mx0 * sl2), mn1 = fmaxf(m[1], mx1 * sl2);
+                const float b0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float b1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
+                m[0] = mn0;
+                m[1] = mn1;
+                const float p0 = fast_exp2(fmaf(s[0], sl2, -b0)), p1 = fast_exp2(fmaf(s[1], sl2, -b1));
+                const float p2 = fast_exp2(fmaf(s[2], sl2, -b0)), p3 = fast_exp2(fmaf(s[3], sl2, -b1));
+                l[0] = fmaf(l[0], al0, p0 + p2);
+                l[1] = fmaf(l[1], al1, p1 + p3);
+                // P^T transposed in registers = the B fragment of V^T P^T
+                // (k = tokens 2 qc, 2 qc + 1 | + 8, + 9; n = head row quad)
+                const uint32_t pb0 = movmatrix_t(pack_half2(p0, p1));
+                const uint32_t pb1 = movmatrix_t(pack_half2(p2, p3));
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-                const float p0 = fast_exp2(fmaf(s[nt][0], sl2, -b0));
-                const float p1 = fast_exp2(fmaf(s[nt][1], sl2, -b0));
-                const float p2 = fast_exp2(fmaf(s[nt][2], sl2, -b1));
-                const float p3 = fast_exp2(fmaf(s[nt][3], sl2, -b1));
-                ps0 += p0 + p1;
-                ps1 += p2 + p3;
-                pa[nt >> 1][(nt & 1) * 2 + 0] = F8 ? pack_half2(p0, p1) : pack_bf16x2(p0, p1);
-                pa[nt >> 1][(nt & 1) * 2 + 1] = F8 ? pack_half2(p2, p3) : pack_bf16x2(p2, p3);
-            }
-            l[0] = fmaf(l[0], al0, ps0);
-            l[1] = fmaf(l[1], al1, ps1);
-#pragma unroll
-            for (int nd = 0; nd < D / 8; ++nd) {
-                o[nd][0] *= al0;
-                o[nd][1] *= al0;
-                o[nd][2] *= al1;
-                o[nd][3] *= al1;
-            }
-            // ---- O += P V, one 16-token k-step at a time
-#pragma unroll
-            for (int ks = 0; ks < MT; ++ks) {
-                const int tk = tok_base + 16 * ks + 2 * qc;
+                for (int nd = 0; nd < D / 16; ++nd) {
+                    o[nd][0] *= al0;
+                    o[nd][1] *= al1;
+                    o[nd][2] *= al0;
+                    o[nd][3] *= al1;
+                }
+                // ---- O^T += V^T P^T: the thread reads dims 16 quad .. + 15 of
+                // tokens tk, tk + 1, tk + 8, tk + 9 (one 16-byte load each);
+                // byte permutes pair the tokens per dim.  Dim tile 2 c + h has
+                // rows quad / quad + 8 = dims 16 quad + 4 c + 2 h / + 1.
+                const int tk = tok_base + 2 * qc;
                 const uint32_t keep_lo = (tk < n_valid ? 0x0000ffffu : 0u) | (tk + 1 < n_valid ? 0xffff0000u : 0u);
                 const uint32_t keep_hi = (tk + 8 < n_valid ? 0x0000ffffu : 0u) | (tk + 9 < n_valid ? 0xffff0000u : 0u);
-                if constexpr (F8) {
-                    // tokens tk, tk+1, tk+8, tk+9 (the B fragment's k rows): a
-                    // thread takes dims 16 quad .. 16 quad + 15 of each, one
-                    // 16-byte load per token (a quarter-warp's loads hit eight
-                    // distinct bank groups under the swizzle); word c holds dims
-                    // 16 quad + 4 c .. +3
-                    const uint4 x0 = ld_shared_v4(vb + swz128(tk, quad));
-                    const uint4 x1 = ld_shared_v4(vb + swz128(tk + 1, quad));
-                    const uint4 x2 = ld_shared_v4(vb + swz128(tk + 8, quad));
-                    const uint4 x3 = ld_shared_v4(vb + swz128(tk + 9, quad));
-                    const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
-                    const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
+                const uint4 x0 = ld_shared_v4(vb + swz128(tk, quad));
+                const uint4 x1 = ld_shared_v4(vb + swz128(tk + 1, quad));
+                const uint4 x2 = ld_shared_v4(vb + swz128(tk + 8, quad));
+                const uint4 x3 = ld_shared_v4(vb + swz128(tk + 9, quad));
+                const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
+                const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        const uint32_t w0 = y0[c], w1 = y1[c], w2 = y2[c], w3 = y3[c];
-                        // byte pairs per dim (dims 0, 1 | dims 2, 3), widened:
-                        // bl[i] = tokens (tk, tk+1) of dim i, bh[i] = (tk+8, tk+9)
-                        uint32_t bl[4], bh[4];
-                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x5140), bl[0], bl[1]);
-                        e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x7362), bl[2], bl[3]);
-                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x5140), bh[0], bh[1]);
-                        e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x7362), bh[2], bh[3]);
+                for (int c = 0; c < D / 32; ++c) {
+                    // lo[i] = dim 16 quad + 4 c + i of tokens (tk, tk + 1),
+                    // hi[i] = the same dim of tokens (tk + 8, tk + 9)
+                    uint32_t lo[4], hi[4];
+                    e4m3x4_to_f16x2x2(__byte_perm(y0[c], y1[c], 0x5140), lo[0], lo[1]);
+                    e4m3x4_to_f16x2x2(__byte_perm(y0[c], y1[c], 0x7362), lo[2], lo[3]);
+                    e4m3x4_to_f16x2x2(__byte_perm(y2[c], y3[c], 0x5140), hi[0], hi[1]);
+                    e4m3x4_to_f16x2x2(__byte_perm(y2[c], y3[c], 0x7362), hi[2], hi[3]);
+                    if (partial) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            uint32_t b0 = bl[i], b1 = bh[i];
-                            if (partial) {
-                                b0 &= keep_lo;
-                                b1 &= keep_hi;
-                            }
-                            mma_f16_16816(o[4 * c + i], pa[ks], b0, b1);
+                            lo[i] &= keep_lo;
+                            hi[i] &= keep_hi;
                         }
                     }
-                    continue;
-                }
 #pragma unroll
-                for (int nd2 = 0; nd2 < D / 16; ++nd2) {
-                    const int mat = lane >> 3;
-                    const uint32_t tok = tok_base + 16 * ks + (mat & 1) * 8 + (lane & 7);
-                    const uint32_t chunk = 2 * nd2 + (mat >> 1);
-                    uint32_t r0, r1, r2, r3;
-                    ldsm_x4_t(vb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
-                    if (partial) {
-                        r0 &= keep_lo;
-                        r2 &= keep_lo;
-                        r1 &= keep_hi;
-                        r3 &= keep_hi;
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t va[4] = {lo[2 * h], lo[2 * h + 1], hi[2 * h], hi[2 * h + 1]};
+                        mma_f16_16816(o[2 * c + h], va, pb0, pb1);
                     }
-                    mma_bf16_16816(o[2 * nd2], pa[ks], r0, r1);
-                    mma_bf16_16816(o[2 * nd2 + 1], pa[ks], r2, r3);
+                }
+            } else {
+                // ---- S = Q K^T over this warp's TPW tokens
+                float s[NT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint32_t tok = tok_base + nt * 8 + (lane & 7);
+                    if constexpr (F8) {
+                        // 8-bit rows of 128 dims: matrix i of the x4 load is the
+                        // 16-dim step 4 kk + i; a thread gets dims 4 qc .. 4 qc + 3.
+                        // Odd steps accumulate apart, so two chains of four
+                        // dependent MMAs run side by side instead of one of eight.
+                        float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int kk = 0; kk < D / 64; ++kk) {
+                            const uint32_t chunk = 4 * kk + (lane >> 3);
+                            uint32_t r[4];
+                            ldsm_x4(kb + swz128(tok, chunk), r[0], r[1], r[2], r[3]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t b0, b1;
+                                e4m3x4_to_f16x2x2(r[i], b0, b1);
+                                mma_f16_16816((i & 1) ? s2 : s[nt], qa[4 * kk + i], b0, b1);
+                            }
+                        }
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) s[nt][e] += s2[e];
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < D / 32; ++kk) {
+                            const uint32_t chunk = 4 * kk + (lane >> 3);
+                            uint32_t r0, r1, r2, r3;
+                            ldsm_x4(kb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
+                            mma_bf16_16816(s[nt], qa[2 * kk], r0, r1);
+                            mma_bf16_16816(s[nt], qa[2 * kk + 1], r2, r3);
+                        }
+                    }
+                }
+                const bool partial = n_valid < kTileTokens;
+                if (partial) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int tk = tok_base + nt * 8 + 2 * qc;
+                        if (tk >= n_valid) s[nt][0] = s[nt][2] = -INFINITY;
+                        if (tk + 1 >= n_valid) s[nt][1] = s[nt][3] = -INFINITY;
+                    }
+                }
+                // ---- online softmax (base 2, scaled) and P fragments
+                float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
+                    mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
+                }
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                const float mn0 = fmaxf(m[0], mx0 * sl2), mn1 = fmaxf(m[1], mx1 * sl2);
+                const float b0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float b1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = fast_exp2(m[0] - b0), al1 = fast_exp2(m[1] - b1);
+                m[0] = mn0;
+                m[1] = mn1;
+                float ps0 = 0.f, ps1 = 0.f;
+                uint32_t pa[MT][4];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float p0 = fast_exp2(fmaf(s[nt][0], sl2, -b0));
+                    const float p1 = fast_exp2(fmaf(s[nt][1], sl2, -b0));
+                    const float p2 = fast_exp2(fmaf(s[nt][2], sl2, -b1));
+                    const float p3 = fast_exp2(fmaf(s[nt][3], sl2, -b1));
+                    ps0 += p0 + p1;
+                    ps1 += p2 + p3;
+                    pa[nt >> 1][(nt & 1) * 2 + 0] = F8 ? pack_half2(p0, p1) : pack_bf16x2(p0, p1);
+                    pa[nt >> 1][(nt & 1) * 2 + 1] = F8 ? pack_half2(p2, p3) : pack_bf16x2(p2, p3);
+                }
+                l[0] = fmaf(l[0], al0, ps0);
+                l[1] = fmaf(l[1], al1, ps1);
+#pragma unroll
+                for (int nd = 0; nd < D / 8; ++nd) {
+                    o[nd][0] *= al0;
+                    o[nd][1] *= al0;
+                    o[nd][2] *= al1;
+                    o[nd][3] *= al1;
+                }
+                // ---- O += P V, one 16-token k-step at a time
+#pragma unroll
+                for (int ks = 0; ks < MT; ++ks) {
+                    const int tk = tok_base + 16 * ks + 2 * qc;
+                    const uint32_t keep_lo = (tk < n_valid ? 0x0000ffffu : 0u) | (tk + 1 < n_valid ? 0xffff0000u : 0u);
+                    const uint32_t keep_hi = (tk + 8 < n_valid ? 0x0000ffffu : 0u) | (tk + 9 < n_valid ? 0xffff0000u : 0u);
+                    if constexpr (F8) {
+                        // tokens tk, tk+1, tk+8, tk+9 (the B fragment's k rows): a
+                        // thread takes dims 16 quad .. 16 quad + 15 of each, one
+                        // 16-byte load per token (a quarter-warp's loads hit eight
+                        // distinct bank groups under the swizzle); word c holds dims
+                        // 16 quad + 4 c .. +3
+                        const uint4 x0 = ld_shared_v4(vb + swz128(tk, quad));
+                        const uint4 x1 = ld_shared_v4(vb + swz128(tk + 1, quad));
+                        const uint4 x2 = ld_shared_v4(vb + swz128(tk + 8, quad));
+                        const uint4 x3 = ld_shared_v4(vb + swz128(tk + 9, quad));
+                        const uint32_t y0[4] = {x0.x, x0.y, x0.z, x0.w}, y1[4] = {x1.x, x1.y, x1.z, x1.w};
+                        const uint32_t y2[4] = {x2.x, x2.y, x2.z, x2.w}, y3[4] = {x3.x, x3.y, x3.z, x3.w};
+#pragma unroll
+                        for (int c = 0; c < D / 32; ++c) {
+                            const uint32_t w0 = y0[c], w1 = y1[c], w2 = y2[c], w3 = y3[c];
+                            // byte pairs per dim (dims 0, 1 | dims 2, 3), widened:
+                            // bl[i] = tokens (tk, tk+1) of dim i, bh[i] = (tk+8, tk+9)
+                            uint32_t bl[4], bh[4];
+                            e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x5140), bl[0], bl[1]);
+                            e4m3x4_to_f16x2x2(__byte_perm(w0, w1, 0x7362), bl[2], bl[3]);
+                            e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x5140), bh[0], bh[1]);
+                            e4m3x4_to_f16x2x2(__byte_perm(w2, w3, 0x7362), bh[2], bh[3]);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                uint32_t b0 = bl[i], b1 = bh[i];
+                                if (partial) {
+                                    b0 &= keep_lo;
+                                    b1 &= keep_hi;
+                                }
+                                mma_f16_16816(o[4 * c + i], pa[ks], b0, b1);
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int nd2 = 0; nd2 < D / 16; ++nd2) {
+                            const int mat = lane >> 3;
+                            const uint32_t tok = tok_base + 16 * ks + (mat & 1) * 8 + (lane & 7);
+                            const uint32_t chunk = 2 * nd2 + (mat >> 1);
+                            uint32_t r0, r1, r2, r3;
+                            ldsm_x4_t(vb + (chunk >> 3) * L::kBoxBytes + swz128(tok, chunk & 7), r0, r1, r2, r3);
+                            if (partial) {
+                                r0 &= keep_lo;
+                                r2 &= keep_lo;
+                                r1 &= keep_hi;
+                                r3 &= keep_hi;
+                            }
+                            mma_bf16_16816(o[2 * nd2], pa[ks], r0, r1);
+                            mma_bf16_16816(o[2 * nd2 + 1], pa[ks], r2, r3);
+                    }
+                    }
                 }
             }
         }
@@ -407,11 +543,22 @@ __global__ void __launch_bounds__(160, 2)
             const int h0 = kvh * a.g + hc * a.hc_rows;
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
-                l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
-                if (qc == 0) {
-                    stat[(warp * 16 + quad + 8 * r) * 2] = m[r];
-                    stat[(warp * 16 + quad + 8 * r) * 2 + 1] = l[r];
+                if constexpr (SW) {
+                    // rows 2 qc + r: the tokens are spread over the quads
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 4);
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 8);
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 16);
+                    if (quad == 0) {
+                        stat[(warp * 16 + 2 * qc + r) * 2] = m[r];
+                        stat[(warp * 16 + 2 * qc + r) * 2 + 1] = l[r];
+                    }
+                } else {
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 1);
+                    l[r] += __shfl_xor_sync(0xffffffffu, l[r], 2);
+                    if (qc == 0) {
+                        stat[(warp * 16 + quad + 8 * r) * 2] = m[r];
+                        stat[(warp * 16 + quad + 8 * r) * 2 + 1] = l[r];
+                    }
                 }
             }
             named_barrier(1, 128);
@@ -432,10 +579,25 @@ __global__ void __launch_bounds__(160, 2)
                 if (warp % WPM == step) {
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const int row = 16 * mt_w + quad + 8 * r;
+                        const int row = SW ? 2 * qc + r : 16 * mt_w + quad + 8 * r;
                         const float M = rowml[row * 2];
                         float sc = (M == -INFINITY) ? 0.f : fast_exp2(m[r] - M);
-                        if constexpr (F8) {
+                        if constexpr (SW) {
+                            // o[nd][r], o[nd][2 + r] = dims 16 quad + 2 nd, + 1 of this row
+                            sc *= __ldg(a.v_scale + kvh);
+                            float* dst = obuf + row * L::kOStride + 16 * quad;
+#pragma unroll
+                            for (int nd = 0; nd < D / 16; nd += 2) {
+                                const float4 v = make_float4(o[nd][r] * sc, o[nd][2 + r] * sc,
+                                                             o[nd + 1][r] * sc, o[nd + 1][2 + r] * sc);
+                                float4* p4 = reinterpret_cast<float4*>(dst + 2 * nd);
+                                if (step == 0) *p4 = v;
+                                else {
+                                    const float4 u = *p4;
+                                    *p4 = make_float4(u.x + v.x, u.y + v.y, u.z + v.z, u.w + v.w);
+                                }
+                            }
+                        } else if constexpr (F8) {
                             // FP8: output tile nd = 4 c + i holds dims 32 qc + 4 c + i (+16)
                             sc *= __ldg(a.v_scale + kvh);
                             float* dst = obuf + row * L::kOStride + 32 * qc;
@@ -451,17 +613,17 @@ __global__ void __launch_bounds__(160, 2)
                                     p0[16] += v1;
                                 }
                             }
-                            continue;
-                        }
-                        float* dst = obuf + row * L::kOStride + 2 * qc;
+                        } else {
+                            float* dst = obuf + row * L::kOStride + 2 * qc;
 #pragma unroll
-                        for (int nd = 0; nd < D / 8; ++nd) {
-                            float2 v = make_float2(o[nd][2 * r] * sc, o[nd][2 * r + 1] * sc);
-                            float2* p2 = reinterpret_cast<float2*>(dst + nd * 8);
-                            if (step == 0) *p2 = v;
-                            else {
-                                float2 u = *p2;
-                                *p2 = make_float2(u.x + v.x, u.y + v.y);
+                            for (int nd = 0; nd < D / 8; ++nd) {
+                                float2 v = make_float2(o[nd][2 * r] * sc, o[nd][2 * r + 1] * sc);
+                                float2* p2 = reinterpret_cast<float2*>(dst + nd * 8);
+                                if (step == 0) *p2 = v;
+                                else {
+                                    float2 u = *p2;
+                                    *p2 = make_float2(u.x + v.x, u.y + v.y);
+                                }
                             }
                         }
                     }
@@ -612,17 +774,24 @@ static int occupancy_gqa_t(int B) {
 
 // Stages per configuration: a 64-token K+V tile is 32 KB at D=128 (16 KB
 // with the FP8 cache), 16 KB at D=64; three (six) of them keep ~96 KB in
-// flight per CTA, two CTAs per SM.
+// flight per CTA, two CTAs per SM.  MT = 0 (FP8, at most 8 head rows) is the
+// transposed form, built twice: two CTAs per SM of six stages, or (dense)
+// three of four stages under a 128-register cap.
 #define KVDEC_GQA_DISPATCH(FN, ...)                                                          \
-    (F8 ? (MT == 1 ? FN<128, 1, 6, true>(__VA_ARGS__) : FN<128, 2, 6, true>(__VA_ARGS__))  \
+    (F8 ? (MT == 0   ? (dense ? FN<128, 0, 4, true>(__VA_ARGS__)                           \
+                              : FN<128, 0, 6, true>(__VA_ARGS__))                          \
+           : MT == 1 ? FN<128, 1, 6, true>(__VA_ARGS__)                                    \
+                     : FN<128, 2, 6, true>(__VA_ARGS__))                                   \
         : D == 128 ? (MT == 1 ? FN<128, 1, 3, false>(__VA_ARGS__) : FN<128, 2, 3, false>(__VA_ARGS__)) \
                    : (MT == 1 ? FN<64, 1, 6, false>(__VA_ARGS__) : FN<64, 2, 6, false>(__VA_ARGS__)))
 
-cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,
+cudaError_t launch_gqa(int D, int MT, bool F8, bool dense, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st) {
     return KVDEC_GQA_DISPATCH(launch_gqa_t, tk, tv, a, grid, st);
 }
 
-int occupancy_gqa(int D, int MT, bool F8, int B) { return KVDEC_GQA_DISPATCH(occupancy_gqa_t, B); }
+int occupancy_gqa(int D, int MT, bool F8, bool dense, int B) {
+    return KVDEC_GQA_DISPATCH(occupancy_gqa_t, B);
+}
 
 }  // namespace kvdec

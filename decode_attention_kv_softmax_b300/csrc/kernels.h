@@ -162,9 +162,11 @@ cudaError_t launch_mla_expand_tc(const MlaExpandMaps& maps, const MlaExpandArgs&
 int max_pairs_mla(int B);
 int max_batch_mla();   // largest batch whose tile table fits in shared memory
 
-cudaError_t launch_gqa(int D, int MT, bool F8, const CUtensorMap& tk, const CUtensorMap& tv,
+// MT: head-row tiles of 16 (1 or 2), or 0 for the transposed FP8 form (at
+// most 8 head rows); dense selects that form's three-CTAs-per-SM build.
+cudaError_t launch_gqa(int D, int MT, bool F8, bool dense, const CUtensorMap& tk, const CUtensorMap& tv,
                        const GqaArgs& a, int grid, cudaStream_t st);
-int occupancy_gqa(int D, int MT, bool F8, int B);
+int occupancy_gqa(int D, int MT, bool F8, bool dense, int B);
 cudaError_t launch_combine(const CombineArgs& a, cudaStream_t st);
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st);
 cudaError_t launch_selftest_wait(uint64_t timeout_ns, uint32_t* err, cudaStream_t st);

@@ -48,6 +48,11 @@ FP8 = [
     (2, 48, 1, [100, 260], False, 0),                       # g = 48: two head chunks
     (3, 64, 8, [5000, 70, 1], True, 0),                     # 70B-shaped, paged
     (2, 16, 1, [129, 2000], True, 5),
+    # group sizes below 8: the head rows fill part of the 8 MMA columns
+    (4, 8, 4, [2, 128, 129, 3000], False, 0),               # g = 2
+    (3, 12, 4, [1, 300, 2000], False, 5),                   # g = 3, pieces merged
+    (2, 10, 2, [65, 900], True, 0),                         # g = 5, paged
+    (2, 14, 2, [64, 1500], False, 3),                       # g = 7
 ]
 
 
@@ -55,6 +60,27 @@ FP8 = [
 def test_fp8_full_parity(cuda_lib, B, h, n_kv, sl, paged, max_ctas):
     case = kvgen.gqa_case(B, h, n_kv, 128, seqlens=sl, paged=paged, seed=700 + B * h,
                           device="cuda", kv_dtype="fp8")
+    out, lse = run(cuda_lib, case, max_ctas=max_ctas)
+    ref, lref = full_oracle(case)
+    assert_attn_close(out, ref, "out")
+    assert_lse_close(lse, lref, "lse")
+
+
+@pytest.mark.parametrize("max_ctas", [0, 7])
+def test_fp8_large_capacity_takes_the_two_cta_form(cuda_lib, max_ctas):
+    """A cache with room for more than 256 tiles per SM runs the transposed
+    form's two-CTA build (six stages per CTA) instead of the three-CTA one.
+    Here the block table is padded with unused columns, so the sequences stay
+    short: the plan's grid, seen through the workspace size, shrinks, and the
+    output still matches the oracle."""
+    case = kvgen.gqa_case(4, 32, 8, 128, seqlens=[1, 65, 700, 3000], paged=True, seed=761,
+                          device="cuda", kv_dtype="fp8")
+    bt = case.block_table
+    ws_short = cuda_lib.gqa_workspace_bytes(case.q, case.k, case.v, case.seqlens, bt)
+    pad = torch.zeros((bt.shape[0], 2048 - bt.shape[1]), dtype=torch.int32, device="cuda")
+    case.block_table = torch.cat([bt, pad], dim=1).contiguous()
+    ws_long = cuda_lib.gqa_workspace_bytes(case.q, case.k, case.v, case.seqlens, case.block_table)
+    assert ws_long < ws_short
     out, lse = run(cuda_lib, case, max_ctas=max_ctas)
     ref, lref = full_oracle(case)
     assert_attn_close(out, ref, "out")

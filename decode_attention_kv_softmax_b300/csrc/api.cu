@@ -241,15 +241,20 @@ kvdec_status plan_gqa(const kvdec_gqa_params* p, GqaPlan& pl) {
     if (p->window < 0) return fail(KVDEC_ERR_INVALID_ARG, "window %d", p->window);
     pl.D = p->head_dim;
     pl.g = p->num_heads / p->num_kv_heads;
+    DeviceInfo di;
+    int dev;
+    if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
+    // Head chunks of up to 32 rows.  With more than 16 heads per KV head and
+    // fewer (sequence, KV head) units than SMs (MQA-like shapes at small
+    // batch), chunks of 16 double the CTAs at work and halve each tile's MMA
+    // work; the sibling chunk reads the same K/V tiles, from L2.
     pl.hc_rows = pl.g <= 32 ? pl.g : 32;
+    if (pl.g > 16 && (long long)p->batch * p->num_kv_heads * ((pl.g + 31) / 32) < di.sm_count) pl.hc_rows = 16;
     pl.n_hc = (pl.g + pl.hc_rows - 1) / pl.hc_rows;
     // row tiles of 16 head rows; an FP8 cache with at most 8 rows per chunk
     // takes the transposed form (the rows as the MMA's 8 columns)
     pl.MT = pl.hc_rows > 16 ? 2 : (pl.f8 && pl.hc_rows <= 8) ? 0 : 1;
     pl.units = p->batch * p->num_kv_heads * pl.n_hc;
-    DeviceInfo di;
-    int dev;
-    if (!device_info(di, dev)) return fail(KVDEC_ERR_CUDA, "no current CUDA device");
     int occ = cached_occupancy(std::make_tuple(dev, pl.f8 ? 2 : 0, pl.D, pl.MT, p->batch),
                                [&] { return kvdec::occupancy_gqa(pl.D, pl.MT, pl.f8, false, p->batch); });
     if (occ < 1) return fail(KVDEC_ERR_CUDA, "GQA kernel does not fit on this device");

@@ -44,8 +44,9 @@ FP8 = [
     (6, 32, 8, [1, 63, 64, 65, 129, 1000], False, 0),
     (6, 32, 8, [1, 63, 64, 65, 129, 1000], False, 7),      # pieces merged across CTAs
     (4, 16, 16, [70, 300, 64, 5], False, 0),                # MHA
-    (3, 32, 1, [33, 700, 1500], False, 3),                  # MQA, g = 32 (two row tiles)
-    (2, 48, 1, [100, 260], False, 0),                       # g = 48: two head chunks
+    (3, 32, 1, [33, 700, 1500], False, 3),                  # MQA, g = 32, few units: chunks of 16
+    (2, 48, 1, [100, 260], False, 0),                       # g = 48: three head chunks of 16
+    (160, 32, 1, [1 + (41 * i) % 300 for i in range(160)], False, 0),  # 160 units: two row tiles
     (3, 64, 8, [5000, 70, 1], True, 0),                     # 70B-shaped, paged
     (2, 16, 1, [129, 2000], True, 5),
     # group sizes below 8: the head rows fill part of the 8 MMA columns

@@ -34,8 +34,10 @@ SMALL = [
     (3, 8, 2, 128, [1, 65, 4000], False),
     (6, 32, 8, 128, [1, 63, 64, 65, 129, 1000], False),
     (4, 16, 16, 128, [70, 300, 64, 5], False),          # MHA
-    (3, 32, 1, 128, [33, 700, 1500], False),            # MQA g = 32
-    (2, 48, 1, 128, [100, 260], False),                 # g = 48: two head chunks
+    (3, 32, 1, 128, [33, 700, 1500], False),            # MQA g = 32, few units: chunks of 16
+    (2, 48, 1, 128, [100, 260], False),                 # g = 48: three head chunks of 16
+    (160, 32, 1, 128, [1 + (37 * i) % 300 for i in range(160)], False),  # 160 units: 32-row chunks
+    (150, 48, 1, 64, [1 + (53 * i) % 200 for i in range(150)], True),    # 32 + 16 rows, d = 64
     (2, 64, 1, 64, [90, 17], False),                    # g = 64, d = 64
     (5, 8, 4, 64, [1, 2, 64, 127, 300], True),
     (3, 64, 8, 128, [5000, 70, 1], True),               # 70B-shaped, paged

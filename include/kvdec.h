@@ -110,7 +110,10 @@ typedef enum kvdec_kv_format { KVDEC_KV_BF16 = 0, KVDEC_KV_FP8_E4M3 = 1 } kvdec_
  * Workspace: at least kvdec_gqa_workspace_bytes(p) bytes, 256-byte aligned,
  * no initialisation needed (split counters are tagged with a per-call epoch).
  * It holds the split partials and their counters; calls that share it must
- * not overlap on the GPU.
+ * not overlap on the GPU.  Its size follows the launch the call will make:
+ * batch, the head counts, head_dim, kv_format, the cache's capacity
+ * (capacity, or max_blocks when paged), window and max_ctas all enter it, so
+ * query it with the same values the decode call will carry.
  */
 typedef struct kvdec_gqa_params {
     const void* q;

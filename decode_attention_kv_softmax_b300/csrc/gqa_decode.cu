@@ -59,7 +59,9 @@ struct GqaSmem {
     static constexpr int kTileBytes = kBoxes * kBoxBytes;     // K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;
     static constexpr int kRows = MT == 0 ? 8 : 16 * MT;        // head rows of a chunk
-    static constexpr int kOStride = D + 8;                    // padded fp32 row
+    // padded fp32 row; in the transposed form a thread writes 16 consecutive
+    // dims of rows 2 qc, 2 qc + 1, and D + 4 spreads those rows over the banks
+    static constexpr int kOStride = MT == 0 ? D + 4 : D + 8;
     static constexpr int kObuf = NS * kStageBytes;
     static constexpr int kStat = kObuf + kRows * kOStride * 4;  // [4 warps][16][2]
     static constexpr int kRowML = kStat + 4 * 16 * 2 * 4;       // [rows][2]

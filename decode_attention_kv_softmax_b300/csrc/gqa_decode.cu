@@ -577,8 +577,13 @@ __global__ void __launch_bounds__(160, (MT == 0 && NS == 4) ? 3 : 2)
                 rowml[tid * 2 + 1] = Lsum;
             }
             named_barrier(1, 128);
+            // The warps of a row tile add their partial O into obuf in WPM
+            // ordered steps, all of them in every step: in step s warp i takes
+            // the output tiles of slice (i + s) mod WPM, so every element is
+            // summed in the same warp order each call.
             for (int step = 0; step < WPM; ++step) {
-                if (warp % WPM == step) {
+                const int part = (warp % WPM + step) % WPM;
+                {
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         const int row = SW ? 2 * qc + r : 16 * mt_w + quad + 8 * r;
@@ -590,6 +595,7 @@ __global__ void __launch_bounds__(160, (MT == 0 && NS == 4) ? 3 : 2)
                             float* dst = obuf + row * L::kOStride + 16 * quad;
 #pragma unroll
                             for (int nd = 0; nd < D / 16; nd += 2) {
+                                if (nd / (D / 16 / WPM) != part) continue;
                                 const float4 v = make_float4(o[nd][r] * sc, o[nd][2 + r] * sc,
                                                              o[nd + 1][r] * sc, o[nd + 1][2 + r] * sc);
                                 float4* p4 = reinterpret_cast<float4*>(dst + 2 * nd);
@@ -605,6 +611,7 @@ __global__ void __launch_bounds__(160, (MT == 0 && NS == 4) ? 3 : 2)
                             float* dst = obuf + row * L::kOStride + 32 * qc;
 #pragma unroll
                             for (int nd = 0; nd < D / 8; ++nd) {
+                                if (nd / (D / 8 / WPM) != part) continue;
                                 float* p0 = dst + 4 * (nd >> 2) + (nd & 3);
                                 const float v0 = o[nd][2 * r] * sc, v1 = o[nd][2 * r + 1] * sc;
                                 if (step == 0) {
@@ -619,6 +626,7 @@ __global__ void __launch_bounds__(160, (MT == 0 && NS == 4) ? 3 : 2)
                             float* dst = obuf + row * L::kOStride + 2 * qc;
 #pragma unroll
                             for (int nd = 0; nd < D / 8; ++nd) {
+                                if (nd / (D / 8 / WPM) != part) continue;
                                 float2 v = make_float2(o[nd][2 * r] * sc, o[nd][2 * r + 1] * sc);
                                 float2* p2 = reinterpret_cast<float2*>(dst + nd * 8);
                                 if (step == 0) *p2 = v;
